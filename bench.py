@@ -1,0 +1,473 @@
+"""Benchmark of one paged-attention layer step on GB300.
+
+Default workload (N=1): the Qwen3-0.6B-shaped decode layer -- 128 sequences,
+16 query / 8 KV heads, head_dim 128, page_size 16, context lengths uniform in
+512..4096 over a randomly permuted pool 1.1x the pages in use.  One step is
+the whole hot path for that batch: kv_store of the 128 new tokens' K/V rows,
+then paged decode attention (main kernel + log-sum-exp merge).
+
+  value     algorithmic HBM bytes of the step / step time (GB/s); inputs
+            resident in HBM; the 1.3 GB KV pool is larger than L2, so no flush
+  e2e       the same bytes over the time of the same step through the public
+            API with host buffers: pinned host -> device copies of the step's
+            inputs, the calls, and the device -> host read of the output
+  roofline  decode call (main + merge kernel) bytes / its CUDA-event time,
+            against the measured HBM copy bandwidth
+  prefill   the ragged-prefill workload (8 requests, 128..2048 new tokens,
+            0-50 % cached prefix) in TFLOP/s against the measured bf16 peak,
+            L2 flushed between repetitions
+  cpu_baseline  the CPU oracle on a bounded sample of the same step
+
+--impl reference times the CPU oracle on the same workload (bounded samples).
+--gpus N under torchrun runs N independent replicas (one per GPU, no
+collective in the data path) and reports the aggregate.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged decode attn HBM GB/s (% of peak) + tokens/s; prefill TFLOP/s (% peak)"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+# ------------------------------------------------------------------ workload accounting
+def decode_bytes(x) -> int:
+    """Algorithmic bytes of one paged decode call: every key/value row of every
+    sequence read once, q read, output written, the page-table entries and
+    seq_lens read."""
+    L = x.seq_lens.astype(np.int64)
+    kv = int(L.sum()) * x.Hkv * x.d * 2 * 2
+    qo = 2 * x.B * x.Hq * x.d * 2
+    pt = int(((L + x.page_size - 1) // x.page_size).sum()) * 4 + x.B * 4
+    return kv + qo + pt
+
+
+def store_bytes(x) -> int:
+    """kv_store: read each new K and V row, write it to its slot, read out_loc."""
+    return 2 * 2 * x.Tq * x.Hkv * x.d * 2 + x.Tq * 4
+
+
+def prefill_flops(x) -> int:
+    """Unmasked QK^T and PV multiply-adds: 4 * d * Hq * sum_r (n_r c_r + n_r (n_r + 1) / 2)."""
+    n = x.new_lens.astype(np.int64)
+    c = x.prefix_lens.astype(np.int64)
+    pairs = int((n * c + n * (n + 1) // 2).sum())
+    return 4 * x.d * x.Hq * pairs
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            j = json.load(open(p))
+            return (float(j["hbm_gbs"]), float(j["bf16_tflops"]),
+                    float(j.get("bf16_tflops_sustained", j["bf16_tflops"])), "measured")
+        except Exception:  # noqa: BLE001
+            pass
+    return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
+
+
+def source_digest(*names) -> str:
+    h = hashlib.sha256()
+    for n in names:
+        h.update(open(os.path.join(ROOT, "paged_kv_cache_out_gb300", "csrc", n), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(summary: str, digest: str):
+    """DRAM bytes per launch from a committed ncu summary, if its source digest matches."""
+    p = os.path.join(ROOT, "profiles", summary)
+    if not os.path.exists(p):
+        return None
+    vals = {}
+    for line in open(p):
+        if ":" in line and line.strip().startswith("- "):
+            k, v = line.strip()[2:].split(":", 1)
+            vals[k.strip()] = v.strip().strip("`")
+    if vals.get("source_digest") != digest:
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            self.f = os.fdopen(fd, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not self.path:
+            return None
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------ GPU arm
+def to_dev(a, dev):
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(a))
+    if a.dtype == np.uint16:
+        t = t.view(torch.int16).view(torch.bfloat16)
+    return t.to(dev)
+
+
+def run_gpu(args, rank, world):
+    import torch
+    import paged_kv_cache_out_gb300 as pkv
+    from synth import make_config
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    pkv.load_library()
+    hbm_peak, bf16_peak, bf16_sus, peak_kind = measured_peaks()
+
+    x = make_config(args.workload, seed=args.seed + rank)
+    assert x.meta["phase"] == "decode", "the GPU arm times a decode workload"
+    stream = torch.cuda.Stream(device=dev)
+    k, v = to_dev(x.k_cache, dev), to_dev(x.v_cache, dev)
+    q, k_new, v_new = to_dev(x.q, dev), to_dev(x.k_new, dev), to_dev(x.v_new, dev)
+    out_loc, pt, sl = to_dev(x.out_loc, dev), to_dev(x.page_table, dev), to_dev(x.seq_lens, dev)
+    out = torch.empty_like(q)
+    ws = pkv.decode_workspace(x.B, x.Hq, x.Hkv, x.d, dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def step():
+        pkv.kv_store(k_new, v_new, out_loc, k, v, dev_status=status, stream=stream)
+        pkv.paged_decode_attn(q, k, v, pt, sl, x.scale, workspace=ws, dev_status=status, out=out,
+                              stream=stream)
+
+    B_dec = decode_bytes(x)
+    B_step = B_dec + store_bytes(x)
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    stream.synchronize()
+    assert int(status.item()) == 0, f"device status {int(status.item())}"
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    # ---- timed region: K steps, per-step events around the decode call too
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index) as clocks:
+        with torch.cuda.stream(stream):
+            t0.record(stream)
+            for i in range(args.steps):
+                pkv.kv_store(k_new, v_new, out_loc, k, v, dev_status=status, stream=stream)
+                ev[i][0].record(stream)
+                pkv.paged_decode_attn(q, k, v, pt, sl, x.scale, workspace=ws, dev_status=status,
+                                      out=out, stream=stream)
+                ev[i][1].record(stream)
+            t1.record(stream)
+        stream.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1) / args.steps
+    dec_ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
+    ms_all = reduce_max(ms, world)
+
+    # ---- end to end through the public API with host buffers
+    pin = lambda a: to_dev(a, "cpu").pin_memory()  # noqa: E731
+    h_in = [pin(x.q), pin(x.k_new), pin(x.v_new), pin(x.out_loc), pin(x.page_table), pin(x.seq_lens)]
+    d_in = [torch.empty_like(t, device=dev) for t in h_in]
+    h_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    h2d = sum(t.numel() * t.element_size() for t in h_in)
+    d2h = h_out.numel() * h_out.element_size()
+
+    def e2e_step():
+        for h, d in zip(h_in, d_in):
+            d.copy_(h, non_blocking=True)
+        pkv.kv_store(d_in[1], d_in[2], d_in[3], k, v, dev_status=status, stream=stream)
+        pkv.paged_decode_attn(d_in[0], k, v, d_in[4], d_in[5], x.scale, workspace=ws,
+                              dev_status=status, out=out, stream=stream)
+        h_out.copy_(out, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            e2e_step()
+        stream.synchronize()
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(stream)
+    stream.synchronize()
+    e2e_ms = reduce_max(e0.elapsed_time(e1) / args.steps, world)
+    assert int(status.item()) == 0
+
+    # ---- prefill TFLOP/s on the ragged-prefill workload (rank 0 reports)
+    prefill = time_prefill(args, dev, stream, bf16_peak, bf16_sus, peak_kind) if rank == 0 else None
+
+    value = world * B_step / (ms_all * 1e-3) / 1e9
+    dec_gbs = B_dec / (dec_ms * 1e-3) / 1e9
+    digest = source_digest("decode.cu", "common.cuh")
+    traffic = profiled_traffic("decode_kernel_qwen3_decode.md", digest)
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_all, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {
+            "workload": f"{args.workload}: B={x.B}, Hq={x.Hq}, Hkv={x.Hkv}, d={x.d}, "
+                        f"page_size={x.page_size}, kv tokens={int(x.seq_lens.sum())}, "
+                        f"pool={x.num_pages} pages; step = kv_store + paged decode",
+            "seed": args.seed,
+            "bytes_per_step": B_step,
+            "l2": "KV pool 1.3 GB > 129 MB L2: inputs larger than L2, no flush",
+            "parallelism": f"replicas x{world}",
+        },
+        "pct_of_peak": round(100.0 * value / world / hbm_peak, 2),
+        "tokens_per_s": round(world * x.B / (ms_all * 1e-3), 1),
+        "roofline": {
+            "bound": "hbm",
+            "kernel": "paged_decode_attn (decode_kernel + decode_merge_kernel)",
+            "achieved": round(dec_gbs, 2),
+            "peak": hbm_peak,
+            "peak_kind": f"{peak_kind} HBM copy GB/s",
+            "unit": "GB/s",
+            "frac": round(dec_gbs / hbm_peak, 4),
+            "traffic": traffic,
+            "algorithmic_bytes": B_dec,
+            "ms": round(dec_ms, 5),
+        },
+        "e2e": {
+            "value": round(world * B_step / (e2e_ms * 1e-3) / 1e9, 2),
+            "unit": "GB/s",
+            "ms_per_step": round(e2e_ms, 5),
+            "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h,
+        },
+        "gpu_launches": 3 * args.steps,
+        "clocks": clocks.summary(),
+    }
+    if prefill is not None:
+        line["prefill"] = prefill
+    return line
+
+
+def time_prefill(args, dev, stream, bf16_peak, bf16_sus, peak_kind):
+    import torch
+    import paged_kv_cache_out_gb300 as pkv
+    from synth import make_config
+
+    x = make_config("ragged_prefill", seed=args.seed)
+    k, v = to_dev(x.k_cache, dev), to_dev(x.v_cache, dev)
+    q, pt, sl, cu = (to_dev(x.q, dev), to_dev(x.page_table, dev), to_dev(x.seq_lens, dev),
+                     to_dev(x.cu_seqlens_q, dev))
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    pkv.kv_store(to_dev(x.k_new, dev), to_dev(x.v_new, dev), to_dev(x.out_loc, dev), k, v,
+                 dev_status=status, stream=stream)
+    out = torch.empty_like(q)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    reps = max(5, args.steps)
+    times = []
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup + reps):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            pkv.paged_prefill_attn(q, cu, k, v, pt, sl, x.scale, x.max_q_len, dev_status=status,
+                                   out=out, stream=stream)
+            b.record(stream)
+            b.synchronize()
+            if i >= args.warmup:
+                times.append(a.elapsed_time(b))
+    assert int(status.item()) == 0
+    ms = statistics.median(times)
+    fl = prefill_flops(x)
+    tf = fl / (ms * 1e-3) / 1e12
+    return {"workload": "ragged_prefill: 8 requests, n~U[128,2048], prefix 0-50 %, Hq=16, "
+                        "Hkv=8, d=128, page_size=16",
+            "tflops": round(tf, 2), "ms": round(ms, 5), "flops": fl,
+            "peak": bf16_peak, "peak_kind": f"{peak_kind} bf16 dense burst",
+            "frac": round(tf / bf16_peak, 4), "l2": "flushed (512 MB write) before each rep"}
+
+
+def reduce_max(v, world):
+    if world <= 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda" if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ CPU oracle
+def oracle_sample(x, target_s: float, threads: int):
+    """Time the oracle (kv_store + attention) on the first sequences of x, growing
+    the sample until it takes about target_s; returns (seconds, bytes, n_seqs)."""
+    import oracle
+    nseq = 1
+    while True:
+        sub = x.subset(0, nseq)
+        t = time.perf_counter()
+        oracle.run_inputs(sub, threads=threads, inplace=True)
+        dt = time.perf_counter() - t
+        if dt >= target_s or nseq >= x.B:
+            return dt, decode_bytes(sub) + store_bytes(sub), nseq
+        nseq = min(x.B, max(nseq + 1, int(nseq * min(8.0, 1.2 * target_s / max(dt, 1e-3)))))
+
+
+def cpu_baseline(x, target_s=12.0):
+    import oracle
+    threads = oracle.max_threads()
+    dt, nbytes, nseq = oracle_sample(x, target_s, threads)
+    reps = 1
+    while dt < target_s and nseq == x.B:          # the whole step is quick: repeat it
+        more, nb, _ = oracle_sample(x, target_s, threads)
+        dt, nbytes, reps = dt + more, nbytes + nb, reps + 1
+    return {"value": round(nbytes / dt / 1e9, 4), "unit": "GB/s", "cores": threads,
+            "kind": "oracle", "seconds": round(dt, 3),
+            "sample": f"kv_store + attention of the first {nseq} of {x.B} sequences, "
+                      f"{reps} time(s) ({nbytes} algorithmic bytes), float64 C, OpenMP over rows"}
+
+
+def run_reference(args):
+    import oracle
+    from synth import make_config
+    oracle.build()
+    x = make_config(args.workload, seed=args.seed)
+    threads = oracle.max_threads()
+    per_step = max(1.0, 20.0 / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        oracle_sample(x, per_step, threads)
+    tot_t, tot_b, nseq = 0.0, 0, 0
+    for _ in range(args.steps):
+        dt, nb, nseq = oracle_sample(x, per_step, threads)
+        tot_t += dt
+        tot_b += nb
+    value = tot_b / tot_t / 1e9
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * tot_t / args.steps, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{args.workload} (bounded samples of the step)", "seed": args.seed},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads,
+                         "kind": "oracle",
+                         "sample": f"each step: kv_store + attention of the first {nseq} of "
+                                   f"{x.B} sequences"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="qwen3_decode",
+                    choices=["tiny_decode", "qwen3_decode", "llama_long_decode"])
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    line = run_gpu(args, rank, world)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            from synth import make_config
+            line["cpu_baseline"] = cpu_baseline(make_config(args.workload, seed=args.seed))
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,187 @@
+/*
+ * pkv.h -- attention over a paged KV cache on NVIDIA GB300 (sm_103a).
+ *
+ * Three operations make up one attention layer of a paged-KV inference step:
+ *
+ *   pkv_kv_store            write this step's new K/V rows into their pool slots
+ *   pkv_paged_decode_attn   one query token per sequence over its cached keys
+ *   pkv_paged_prefill_attn  ragged causal attention of new tokens over a
+ *                           cached prefix plus themselves
+ *
+ * Sources of the operations' meaning:
+ *   - mini-sglang "Engine Class": forward_batch takes a batch whose phase is
+ *     prefill or decode and which carries out_loc (the cache slot of every new
+ *     token); the engine's page_table maps logical to physical KV locations;
+ *     its KV pool is paged (page_size 16 in the example config).
+ *   - miniVLLM "Engine Architecture": prepare_prefill builds cu_seqlens_q
+ *     (cumulative new-token counts, e.g. [0, 5, 8, 12]), slot_mapping and
+ *     block_tables, skipping the num_cached_tokens of each sequence;
+ *     prepare_decode builds context_lens, slot_mapping and block_tables;
+ *     allocate_kv_cache lays each layer's K and V out as
+ *     [num_blocks, block_size, num_kv_heads, head_dim].
+ *   - miniVLLM "LLMEngine": model shapes with num_heads query heads sharing
+ *     num_kv_heads KV heads (grouped-query attention), block_size 256.
+ *
+ * Conventions shared by every call:
+ *   - bf16 tensors are passed as raw 16-bit patterns (pkv_bf16); all tensor
+ *     pointers are DEVICE pointers owned by the caller, dense and C-contiguous
+ *     in the layouts stated below, and 16-byte aligned.  The library never
+ *     allocates, frees or keeps device memory.
+ *   - The KV pool of one layer is k_cache and v_cache, each
+ *     [num_pages, page_size, num_kv_heads, head_dim]; pool slot s is row s of
+ *     the pool viewed as [num_pages * page_size, num_kv_heads, head_dim].
+ *     Token position j of request r lives in slot
+ *         page_table[r * page_table_stride + j / page_size] * page_size + j % page_size.
+ *   - Query head h reads KV head h / (num_q_heads / num_kv_heads).
+ *   - seq_lens[r] counts ALL keys request r attends to after this step's new
+ *     tokens were stored: its cached prefix plus its new tokens.  kv_store must
+ *     therefore run before the attention call that reads those tokens.
+ *   - Pool slots holding no token of the request are never read, so their
+ *     contents (even NaN) do not matter.
+ *   - stream is a cudaStream_t (NULL = the legacy default stream).  Every call
+ *     is asynchronous on that stream and does no host synchronisation; the
+ *     launch configuration depends only on host arguments, never on device
+ *     data, so the calls can be captured in a CUDA graph.
+ *   - Errors the host can see (null pointers, bad sizes, unsupported shapes,
+ *     misalignment, workspace too small) return a pkv_status at once and launch
+ *     nothing.  Errors only the device can see (a page id outside the pool, a
+ *     seq_len beyond the page-table row, a slot beyond the pool, bad
+ *     cu_seqlens_q) are OR-ed as PKV_DEV_* bits into *dev_status when
+ *     dev_status is not NULL; the affected rows are then skipped (kv_store) or
+ *     written as NaN (attention), and nothing outside the caller's buffers is
+ *     ever touched.  The kernels never trap.
+ *   - Supported: head_dim 64 or 128; num_q_heads / num_kv_heads in {1, 2, 4, 8};
+ *     page_size a power of two from 1 to 256.
+ */
+#ifndef PKV_H
+#define PKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t pkv_bf16;
+
+typedef enum pkv_status {
+    PKV_OK = 0,
+    PKV_EINVAL = 1,        /* bad argument: null pointer, size, alignment, workspace */
+    PKV_EUNSUPPORTED = 2,  /* valid but not built: head_dim, GQA ratio, page_size, batch */
+    PKV_ECUDA = 3,         /* a CUDA runtime call failed (launch, attribute, device query) */
+} pkv_status;
+
+/* Bits OR-ed into *dev_status by the kernels. */
+#define PKV_DEV_BAD_SLOT    1  /* out_loc[t] >= num_pages * page_size: row not stored */
+#define PKV_DEV_BAD_PAGE    2  /* a page id outside [0, num_pages): rows written as NaN */
+#define PKV_DEV_BAD_SEQLEN  4  /* seq_len < 0, > page_table_stride * page_size, or < new tokens */
+#define PKV_DEV_BAD_CUSEQ   8  /* cu_seqlens_q not monotone, not starting at 0, or new
+                                  tokens beyond max_q_len / total_q_tokens */
+#define PKV_DEV_TIMEOUT    16  /* an internal pipeline wait gave up (should never happen) */
+
+/* Human-readable name of a pkv_status value. */
+const char *pkv_status_string(int status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int pkv_version(void);
+
+/*
+ * kv_store: copy each new token's K and V rows into its pool slot.
+ *
+ * mini-sglang "Engine Class" (forward_batch, out_loc) and miniVLLM "Engine
+ * Architecture" (slot_mapping: the physical cache slot each new token is
+ * written to; allocate_kv_cache: the pool layout).
+ *
+ *   k_new, v_new  [num_tokens, num_kv_heads, head_dim] bf16, read
+ *   out_loc       [num_tokens] int32: destination slot, or < 0 to skip the
+ *                 token (padding).  Two tokens with the same slot are a
+ *                 caller error: which one lands is unspecified.
+ *   k_cache, v_cache  the pool, [num_pages, page_size, num_kv_heads, head_dim],
+ *                 written only at the listed slots, bit for bit.
+ *   dev_status    optional device int32: PKV_DEV_BAD_SLOT when a slot is
+ *                 >= num_pages * page_size (that token is skipped).
+ * num_tokens == 0 is a no-op.
+ */
+pkv_status pkv_kv_store(const pkv_bf16 *k_new, const pkv_bf16 *v_new,
+                        const int32_t *out_loc, int64_t num_tokens,
+                        pkv_bf16 *k_cache, pkv_bf16 *v_cache,
+                        int64_t num_pages, int page_size, int num_kv_heads,
+                        int head_dim, int32_t *dev_status, void *stream);
+
+/*
+ * Bytes of device workspace pkv_paged_decode_attn needs for these sizes on
+ * the current device (partial softmax results of sequences whose keys are
+ * split over several thread blocks, and the per-batch tile offsets).
+ * Returns 0 for invalid sizes.
+ */
+size_t pkv_decode_workspace_size(int batch, int num_q_heads, int num_kv_heads,
+                                 int head_dim);
+
+/*
+ * paged_decode_attn: one new query token per sequence attends to all
+ * seq_lens[b] keys of its sequence (including its own, stored by kv_store).
+ *
+ * miniVLLM "Engine Architecture", prepare_decode: each sequence contributes
+ * one token; context_lens holds the tokens processed so far; block_tables
+ * give the physical block of each logical block.
+ *
+ *   q             [batch, num_q_heads, head_dim] bf16
+ *   k_cache, v_cache  pool as above
+ *   page_table    int32 rows of page_table_stride entries, row b for sequence b;
+ *                 entries past ceil(seq_lens[b] / page_size) are never read
+ *   seq_lens      [batch] int32, keys per sequence; 0 gives a zero output row
+ *   softmax_scale multiplies q.k before the softmax (1/sqrt(head_dim) usually)
+ *   workspace     device buffer of at least
+ *                 pkv_decode_workspace_size(batch, num_q_heads, num_kv_heads,
+ *                 head_dim) bytes, 16-byte aligned, no initial contents needed;
+ *                 two calls in flight at once need two workspaces
+ *   out           [batch, num_q_heads, head_dim] bf16:
+ *                 out[b,h] = sum_j softmax_j(scale * q[b,h].k_j) v_j
+ *                 accumulated in fp32 and rounded to bf16
+ * batch must be <= 4096.
+ */
+pkv_status pkv_paged_decode_attn(const pkv_bf16 *q, const pkv_bf16 *k_cache,
+                                 const pkv_bf16 *v_cache, const int32_t *page_table,
+                                 int64_t page_table_stride, const int32_t *seq_lens,
+                                 int batch, int num_q_heads, int num_kv_heads,
+                                 int head_dim, int page_size, int64_t num_pages,
+                                 float softmax_scale, void *workspace,
+                                 size_t workspace_bytes, int32_t *dev_status,
+                                 pkv_bf16 *out, void *stream);
+
+/*
+ * paged_prefill_attn: causal attention of each request's new tokens over its
+ * cached prefix and themselves.
+ *
+ * miniVLLM "Engine Architecture", prepare_prefill: the new tokens of all
+ * requests are concatenated (cached prefix tokens excluded) with offsets
+ * cu_seqlens_q; block_tables map logical to physical blocks.  zero-to-sglang
+ * "Chapter 1 mini-sglang: What an Inference Engine Looks Like", section on
+ * Req: a request's extend length is its current length minus its cached
+ * length.
+ *
+ *   q             [total_q_tokens, num_q_heads, head_dim] bf16
+ *   cu_seqlens_q  [batch + 1] int32, cu_seqlens_q[0] = 0, non-decreasing;
+ *                 request r owns new tokens cu_seqlens_q[r] .. cu_seqlens_q[r+1]-1
+ *   seq_lens      [batch] int32: cached prefix c_r plus new tokens n_r
+ *   max_q_len     host upper bound on every n_r (sizes the launch grid)
+ *   out           [total_q_tokens, num_q_heads, head_dim] bf16: new token i of
+ *                 request r (absolute position c_r + i) attends keys
+ *                 0 .. c_r + i; accumulated in fp32, rounded to bf16
+ * Other arguments as for pkv_paged_decode_attn.
+ */
+pkv_status pkv_paged_prefill_attn(const pkv_bf16 *q, const int32_t *cu_seqlens_q,
+                                  const pkv_bf16 *k_cache, const pkv_bf16 *v_cache,
+                                  const int32_t *page_table, int64_t page_table_stride,
+                                  const int32_t *seq_lens, int batch,
+                                  int64_t total_q_tokens, int max_q_len,
+                                  int num_q_heads, int num_kv_heads, int head_dim,
+                                  int page_size, int64_t num_pages, float softmax_scale,
+                                  int32_t *dev_status, pkv_bf16 *out, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H */

@@ -142,10 +142,11 @@ def attention(q, cu_seqlens_q, k_cache, v_cache, page_table, seq_lens, scale,
     return (out, lse) if return_lse else out
 
 
-def run_inputs(x, rows=None, threads: int = 1, return_lse: bool = False):
-    """kv_store of ``x``'s new tokens into copies of its pool, then attention."""
-    k_cache = x.k_cache.copy()
-    v_cache = x.v_cache.copy()
+def run_inputs(x, rows=None, threads: int = 1, return_lse: bool = False, inplace: bool = False):
+    """kv_store of ``x``'s new tokens into copies of its pool (or into the pool
+    itself when ``inplace``), then attention."""
+    k_cache = x.k_cache if inplace else x.k_cache.copy()
+    v_cache = x.v_cache if inplace else x.v_cache.copy()
     kv_store(x.k_new, x.v_new, x.out_loc, k_cache, v_cache)
     return attention(x.q, x.cu_seqlens_q, k_cache, v_cache, x.page_table, x.seq_lens,
                      x.scale, rows=rows, threads=threads, return_lse=return_lse)

@@ -1,0 +1,617 @@
+// decode.cu -- paged decode attention: one query token per sequence over all
+// of its cached keys, read through the page table.
+//
+// miniVLLM "Engine Architecture", prepare_decode: every sequence contributes
+// one token; context_lens counts its keys; block_tables map each logical block
+// to a physical one.  Grouped-query attention: the num_q_heads / num_kv_heads
+// query heads of one KV head share its K/V rows (miniVLLM "LLMEngine":
+// num_heads, num_kv_heads).
+//
+// Design (memory-bound: ~2 flops per byte of K/V):
+//  * Work is measured in tiles of T key tokens of one (sequence, KV head)
+//    "segment".  All segments are laid end to end and cut into gridDim.x equal
+//    ranges, one per persistent block, so every block streams the same number
+//    of bytes however unequal the sequence lengths are.  A segment cut by a
+//    range boundary yields partial softmax states (max, sum, weighted values)
+//    in the workspace; a second kernel merges them by log-sum-exp.
+//  * One producer warp walks the block's tiles and stages each page's K and V
+//    rows for this KV head into shared memory with TMA tensor copies (one box
+//    of min(page_size, T) rows per page), through a ring of mbarrier-tracked
+//    stages.  K/V are streamed once, so the copies carry an L2 evict-first hint.
+//  * Four consumer warps split every tile by rows: head_dim/8 lanes hold one
+//    16-byte slice of a row; each lane keeps the G query heads' slice of q in
+//    registers (pre-multiplied by scale*log2 e), reduces dot products with
+//    warp shuffles, keeps its own online-softmax state per head, and
+//    accumulates its slice of the output.  At the end of a segment piece the
+//    row-groups' states are merged through shared memory.
+#include <math.h>
+
+#include <mutex>
+
+#include "common.cuh"
+
+namespace pkv {
+namespace decode {
+
+constexpr int kConsumerWarps = 4;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;  // warps 0-3 consume, warp 4 produces
+constexpr int kMaxBatch = 4096;
+constexpr int kCtasPerSm = 2;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kNegBig = -1.0e30f;  // running-max start: finite, so 2^(m - m') never is NaN
+
+template <int D>
+struct Shape {
+    static constexpr int T = (D == 128) ? 32 : 64;  // key tokens per tile
+    static constexpr int R = D / 8;                  // lanes per K/V row (16 B each)
+    static constexpr int ROWS_PER_WARP = 32 / R;
+    static constexpr int GROUPS = kConsumerWarps * ROWS_PER_WARP;
+    static constexpr int U = T / GROUPS;  // rows of a tile per row-group
+    static constexpr int TILE_BYTES = T * D * 2;
+    static constexpr int STAGES = 4;
+};
+
+template <int D, int G>
+struct Smem {
+    using S = Shape<D>;
+    static constexpr int Q_BYTES = ((G * D * 2 + 127) / 128) * 128;
+    static constexpr int STAGE_BYTES = 2 * S::TILE_BYTES + Q_BYTES;
+    static constexpr int RING = S::STAGES * STAGE_BYTES;
+    static constexpr int RED_O = S::GROUPS * G * D * 4;
+    static constexpr int RED_ML = S::GROUPS * G * 2 * 4;
+    static constexpr int BARS = 2 * S::STAGES * 8;
+    static constexpr int FLAGS = S::STAGES * 4 + 16;
+    static constexpr int FIXED = RING + RED_O + RED_ML + BARS + FLAGS;
+    static size_t bytes(int batch) {
+        return 1024 /* alignment slack */ + FIXED + static_cast<size_t>(batch + 1) * 4;
+    }
+};
+
+// Geometry of the balanced partition, shared by the main and merge kernels.
+struct Part {
+    int64_t W;   // total tiles
+    int grid;    // blocks of the main kernel
+    __device__ __forceinline__ int64_t start(int k) const { return (int64_t)k * W / grid; }
+    __device__ __forceinline__ int block_of(int64_t x) const {
+        return static_cast<int>(((x + 1) * grid - 1) / W);
+    }
+};
+
+__device__ __forceinline__ int ntiles_of(int L, int64_t cap, int T) {
+    return (L > 0 && L <= cap) ? (L + T - 1) / T : 0;
+}
+
+// Largest b in [0, B) with prefix[b] <= x (x < prefix[B]).
+__device__ __forceinline__ int owner_search(const int32_t *prefix, int B, int64_t x) {
+    int lo = 0, hi = B;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (prefix[mid] <= x) lo = mid; else hi = mid;
+    }
+    return lo;
+}
+
+struct Piece {
+    int b, g;
+    int t0, t1;         // tile range inside the segment
+    bool whole;         // covers the whole segment
+    bool block_first;   // first piece of this block
+};
+
+__device__ __forceinline__ bool next_piece(int64_t &pos, int64_t end, int64_t block_start,
+                                           const int32_t *prefix, int B, int Hkv, Piece &p) {
+    if (pos >= end) return false;
+    const int b = owner_search(prefix, B, pos);
+    const int nt = (prefix[b + 1] - prefix[b]) / Hkv;
+    const int64_t rel = pos - prefix[b];
+    p.b = b;
+    p.g = static_cast<int>(rel / nt);
+    p.t0 = static_cast<int>(rel % nt);
+    const int64_t seg_end = prefix[b] + (int64_t)(p.g + 1) * nt;
+    const int64_t pend = end < seg_end ? end : seg_end;
+    p.t1 = p.t0 + static_cast<int>(pend - pos);
+    p.whole = (p.t0 == 0) && (pend == seg_end);
+    p.block_first = (pos == block_start);
+    pos = pend;
+    return true;
+}
+
+// Block-wide exclusive scan: prefix[b] = Hkv * sum_{b' < b} ntiles(b').
+__device__ void build_prefix(int32_t *prefix, const int32_t *seq_lens, int B, int Hkv,
+                             int64_t cap, int T, int32_t *scratch /* kThreads/32 + 1 ints */) {
+    const int tid = threadIdx.x;
+    const int per = (B + kThreads - 1) / kThreads;
+    const int lo = tid * per;
+    const int hi = min(B, lo + per);
+    int local = 0;
+    for (int b = lo; b < hi; ++b) local += ntiles_of(seq_lens[b], cap, T) * Hkv;
+    // inclusive scan of `local` over the block
+    const int lane = tid & 31, warp = tid >> 5;
+    int v = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += n;
+    }
+    if (lane == 31) scratch[warp] = v;
+    __syncthreads();
+    if (tid == 0) {
+        int acc = 0;
+        for (int w = 0; w < kThreads / 32; ++w) {
+            const int t = scratch[w];
+            scratch[w] = acc;
+            acc += t;
+        }
+        scratch[kThreads / 32] = acc;
+    }
+    __syncthreads();
+    int run = scratch[warp] + v - local;  // exclusive prefix of this thread's chunk
+    for (int b = lo; b < hi; ++b) {
+        prefix[b] = run;
+        run += ntiles_of(seq_lens[b], cap, T) * Hkv;
+    }
+    if (tid == 0) prefix[B] = scratch[kThreads / 32];
+    __syncthreads();
+}
+
+template <int D, int G>
+__global__ void __launch_bounds__(kThreads, 1)
+    decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                  const __nv_bfloat16 *__restrict__ q, const int32_t *__restrict__ page_table,
+                  int64_t pt_stride, const int32_t *__restrict__ seq_lens, int B, int Hkv,
+                  int ps_log2, int box_rows, int64_t num_pages, float scale_log2,
+                  float *__restrict__ ws_part, int32_t *__restrict__ ws_prefix,
+                  int32_t *dev_status, __nv_bfloat16 *__restrict__ out) {
+    using S = Shape<D>;
+    using M = Smem<D, G>;
+    constexpr int T = S::T, R = S::R, U = S::U, GROUPS = S::GROUPS, STAGES = S::STAGES;
+    const int Hq = Hkv * G;
+    const int64_t cap = pt_stride << ps_log2;
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~uintptr_t(1023));
+    uint8_t *ring = smem;
+    float *red_o = reinterpret_cast<float *>(smem + M::RING);
+    float *red_ml = reinterpret_cast<float *>(smem + M::RING + M::RED_O);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + M::RING + M::RED_O + M::RED_ML);
+    int *flags = reinterpret_cast<int *>(smem + M::RING + M::RED_O + M::RED_ML + M::BARS);
+    volatile int *abort_flag = flags + STAGES;
+    int32_t *prefix = reinterpret_cast<int32_t *>(smem + M::FIXED);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (tid == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(smem_u32(&bars[s]), 1);                        // full: producer + tx bytes
+            mbar_init(smem_u32(&bars[STAGES + s]), kConsumerWarps);  // empty: one per consumer warp
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    // red_ml doubles as the scan scratch before any piece is reduced
+    build_prefix(prefix, seq_lens, B, Hkv, cap, T, reinterpret_cast<int32_t *>(red_ml));
+    if (blockIdx.x == 0)
+        for (int b = tid; b <= B; b += kThreads) ws_prefix[b] = prefix[b];
+
+    Part part{prefix[B], static_cast<int>(gridDim.x)};
+    if (part.W == 0) return;
+    const int64_t my_start = part.start(blockIdx.x);
+    const int64_t my_end = part.start(blockIdx.x + 1);
+    if (my_start >= my_end) return;
+
+    if (warp == kConsumerWarps) {
+        // ------------------------------------------------------------ producer
+        const uint64_t policy = l2_evict_first_policy();
+        if (lane == 0) {
+            prefetch_tmap(&kmap);
+            prefetch_tmap(&vmap);
+        }
+        const int ps_mask = (1 << ps_log2) - 1;
+        const uint32_t box_bytes = static_cast<uint32_t>(box_rows) * D * 2;
+        int64_t pos = my_start;
+        Piece p;
+        uint32_t it = 0;
+        bool ok = true;
+        while (ok && next_piece(pos, my_end, my_start, prefix, B, Hkv, p)) {
+            const int L = seq_lens[p.b];
+            const int32_t *prow = page_table + (int64_t)p.b * pt_stride;
+            for (int tile = p.t0; tile < p.t1; ++tile, ++it) {
+                const int s = it % STAGES;
+                const uint32_t ph = (it / STAGES) & 1;
+                if (it >= STAGES && !mbar_wait_warp(smem_u32(&bars[STAGES + s]), ph ^ 1, abort_flag,
+                                               dev_status)) {
+                    ok = false;
+                    break;
+                }
+                const int tok0 = tile * T;
+                const int ntok = min(T, L - tok0);
+                const int nbox = (ntok + box_rows - 1) / box_rows;
+                // page ids of this tile's boxes (at most T boxes: two per lane)
+                int pg[2] = {0, 0};
+                bool bad = false;
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                    const int i = lane + 32 * k;
+                    if (i < nbox) {
+                        pg[k] = prow[(tok0 + i * box_rows) >> ps_log2];
+                        if (pg[k] < 0 || pg[k] >= num_pages) bad = true;
+                    }
+                }
+                bad = __any_sync(0xffffffffu, bad);
+                const bool first = (tile == p.t0);
+                const uint32_t bytes = (bad ? 0u : 2u * box_bytes * nbox) +
+                                       (first ? static_cast<uint32_t>(G * D * 2) : 0u);
+                uint8_t *st = ring + s * M::STAGE_BYTES;
+                const uint32_t full = smem_u32(&bars[s]);
+                if (lane == 0) {
+                    flags[s] = bad ? 1 : 0;
+                    mbar_arrive_expect_tx(full, bytes);
+                }
+                __syncwarp();
+                if (!bad) {
+#pragma unroll
+                    for (int k = 0; k < 2; ++k) {
+                        const int i = lane + 32 * k;
+                        if (i < nbox) {
+                            const int j = tok0 + i * box_rows;
+                            const int row = (pg[k] << ps_log2) + (j & ps_mask);
+                            tma_load_3d(smem_u32(st + i * box_bytes), &kmap, full, 0, p.g, row,
+                                        policy);
+                            tma_load_3d(smem_u32(st + S::TILE_BYTES + i * box_bytes), &vmap, full,
+                                        0, p.g, row, policy);
+                        }
+                    }
+                }
+                if (first && lane == 0)
+                    bulk_load(smem_u32(st + 2 * S::TILE_BYTES),
+                              q + ((int64_t)p.b * Hq + (int64_t)p.g * G) * D, G * D * 2, full);
+            }
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------------- consumers
+    const int grp = warp * S::ROWS_PER_WARP + lane / R;  // row-group of this lane
+    const int lr = lane % R;                             // 16-byte slice within a row
+    const int ctid = tid;                                // 0..127
+    float qf[G][8];
+    float m[G], l[G], o[G][8];
+    int64_t pos = my_start;
+    Piece p;
+    uint32_t it = 0;
+    bool ok = true;
+    while (ok && next_piece(pos, my_end, my_start, prefix, B, Hkv, p)) {
+        const int L = seq_lens[p.b];
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+            m[h] = kNegBig;
+            l[h] = 0.f;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) o[h][e] = 0.f;
+        }
+        bool bad_piece = false;
+        for (int tile = p.t0; tile < p.t1; ++tile, ++it) {
+            const int s = it % STAGES;
+            const uint32_t ph = (it / STAGES) & 1;
+            if (!mbar_wait_warp(smem_u32(&bars[s]), ph, abort_flag, dev_status)) {
+                ok = false;
+                break;
+            }
+            const uint8_t *st = ring + s * M::STAGE_BYTES;
+            const uint32_t kbase = smem_u32(st);
+            const uint32_t vbase = kbase + S::TILE_BYTES;
+            if (flags[s]) bad_piece = true;
+            if (tile == p.t0) {
+                const uint32_t qbase = kbase + 2 * S::TILE_BYTES;
+#pragma unroll
+                for (int h = 0; h < G; ++h) {
+                    const uint4 w = lds128(qbase + (h * D + lr * 8) * 2);
+                    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        qf[h][2 * e] = bf16lo(ws[e]) * scale_log2;
+                        qf[h][2 * e + 1] = bf16hi(ws[e]) * scale_log2;
+                    }
+                }
+            }
+            const int tok0 = tile * T;
+            float sc[U][G];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int row = grp + u * GROUPS;
+                const uint4 w = lds128(kbase + (row * D + lr * 8) * 2);
+                const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+                float kf[8];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    kf[2 * e] = bf16lo(ws[e]);
+                    kf[2 * e + 1] = bf16hi(ws[e]);
+                }
+#pragma unroll
+                for (int h = 0; h < G; ++h) {
+                    float acc = 0.f;
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) acc = fmaf(qf[h][e], kf[e], acc);
+                    sc[u][h] = acc;
+                }
+            }
+#pragma unroll
+            for (int off = R / 2; off >= 1; off >>= 1) {
+#pragma unroll
+                for (int u = 0; u < U; ++u)
+#pragma unroll
+                    for (int h = 0; h < G; ++h)
+                        sc[u][h] += __shfl_xor_sync(0xffffffffu, sc[u][h], off);
+            }
+            bool valid[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) valid[u] = (tok0 + grp + u * GROUPS) < L;
+            float pr[U][G];
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                float mt = kNegBig;
+#pragma unroll
+                for (int u = 0; u < U; ++u)
+                    if (valid[u]) mt = fmaxf(mt, sc[u][h]);
+                const float mn = fmaxf(m[h], mt);
+                const float alpha = ex2(m[h] - mn);
+                m[h] = mn;
+                float sum = 0.f;
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    pr[u][h] = valid[u] ? ex2(sc[u][h] - mn) : 0.f;
+                    sum += pr[u][h];
+                }
+                l[h] = l[h] * alpha + sum;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) o[h][e] *= alpha;
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int row = grp + u * GROUPS;
+                const uint4 w = lds128(vbase + (row * D + lr * 8) * 2);
+                const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+                float vf[8];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    // rows past the sequence end hold stale data: select, never multiply
+                    vf[2 * e] = valid[u] ? bf16lo(ws[e]) : 0.f;
+                    vf[2 * e + 1] = valid[u] ? bf16hi(ws[e]) : 0.f;
+                }
+#pragma unroll
+                for (int h = 0; h < G; ++h)
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) o[h][e] = fmaf(pr[u][h], vf[e], o[h][e]);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&bars[STAGES + s]));
+        }
+        if (!ok) break;
+
+        // ---- merge the row-groups' states of this piece
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) red_o[(grp * G + h) * D + lr * 8 + e] = o[h][e];
+            if (lr == 0) {
+                red_ml[(grp * G + h) * 2 + 0] = m[h];
+                red_ml[(grp * G + h) * 2 + 1] = l[h];
+            }
+        }
+        named_bar_sync(1, kConsumerWarps * 32);
+        const int slot = static_cast<int>(blockIdx.x) * 2 + (p.block_first ? 0 : 1);
+        for (int idx = ctid; idx < G * D; idx += kConsumerWarps * 32) {
+            const int h = idx / D;
+            float mx = kNegBig;
+#pragma unroll
+            for (int g2 = 0; g2 < GROUPS; ++g2) mx = fmaxf(mx, red_ml[(g2 * G + h) * 2]);
+            float sum = 0.f, acc = 0.f;
+#pragma unroll
+            for (int g2 = 0; g2 < GROUPS; ++g2) {
+                const float w = ex2(red_ml[(g2 * G + h) * 2] - mx);
+                sum = fmaf(red_ml[(g2 * G + h) * 2 + 1], w, sum);
+                acc = fmaf(red_o[(g2 * G + h) * D + (idx % D)], w, acc);
+            }
+            if (p.whole) {
+                const float v = bad_piece ? __int_as_float(0x7fc00000) : acc / sum;
+                out[((int64_t)p.b * Hq + (int64_t)p.g * G) * D + idx] = __float2bfloat16_rn(v);
+            } else {
+                float *part_o = ws_part + (int64_t)slot * (G * D + 2 * G);
+                part_o[idx] = acc;
+                if (idx % D == 0) {
+                    part_o[G * D + 2 * h] = bad_piece ? __int_as_float(0x7fc00000) : mx;
+                    part_o[G * D + 2 * h + 1] = sum;
+                }
+            }
+        }
+        if (bad_piece && ctid == 0 && dev_status) atomicOr(dev_status, PKV_DEV_BAD_PAGE);
+        named_bar_sync(1, kConsumerWarps * 32);
+    }
+}
+
+// Merge of the partial states of segments that were cut across blocks, and
+// the output of segments with no keys (zeros, or NaN for an invalid length).
+template <int D, int G>
+__global__ void __launch_bounds__(128)
+    decode_merge_kernel(const int32_t *__restrict__ seq_lens, const int32_t *__restrict__ ws_prefix,
+                        const float *__restrict__ ws_part, int B, int Hkv, int64_t cap, int grid,
+                        int32_t *dev_status, __nv_bfloat16 *__restrict__ out) {
+    using S = Shape<D>;
+    const int b = blockIdx.x / Hkv, g = blockIdx.x % Hkv;
+    const int Hq = Hkv * G;
+    __nv_bfloat16 *orow = out + ((int64_t)b * Hq + (int64_t)g * G) * D;
+    const int nt = (ws_prefix[b + 1] - ws_prefix[b]) / Hkv;
+    if (nt == 0) {
+        const int L = seq_lens[b];
+        const bool bad = (L < 0 || L > cap);
+        if (bad && g == 0 && threadIdx.x == 0 && dev_status) atomicOr(dev_status, PKV_DEV_BAD_SEQLEN);
+        for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x)
+            orow[idx] = __float2bfloat16_rn(bad ? __int_as_float(0x7fc00000) : 0.f);
+        return;
+    }
+    Part part{ws_prefix[B], grid};
+    const int64_t s0 = ws_prefix[b] + (int64_t)g * nt;
+    const int64_t s1 = s0 + nt;
+    const int k0 = part.block_of(s0), k1 = part.block_of(s1 - 1);
+    if (k0 == k1) return;  // written directly by the main kernel
+    (void)S::T;
+    // Blocks k0 < k <= k1 whose range is empty (fewer tiles than blocks) hold
+    // no partial state of this segment and are skipped.
+    for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
+        const int h = idx / D;
+        float mx = kNegBig;
+        bool bad = false;
+        for (int k = k0; k <= k1; ++k) {
+            if (part.start(k + 1) <= part.start(k)) continue;
+            const int slot = 2 * k + ((k == k0 && s0 != part.start(k0)) ? 1 : 0);
+            const float mk = ws_part[(int64_t)slot * (G * D + 2 * G) + G * D + 2 * h];
+            bad |= isnan(mk);
+            mx = fmaxf(mx, mk);
+        }
+        float sum = 0.f, acc = 0.f;
+        for (int k = k0; k <= k1; ++k) {
+            if (part.start(k + 1) <= part.start(k)) continue;
+            const int slot = 2 * k + ((k == k0 && s0 != part.start(k0)) ? 1 : 0);
+            const float *pk = ws_part + (int64_t)slot * (G * D + 2 * G);
+            const float w = ex2(pk[G * D + 2 * h] - mx);
+            sum = fmaf(pk[G * D + 2 * h + 1], w, sum);
+            acc = fmaf(pk[idx], w, acc);
+        }
+        orow[idx] = __float2bfloat16_rn(bad ? __int_as_float(0x7fc00000) : acc / sum);
+    }
+}
+
+// ---------------------------------------------------------------- host side
+struct LaunchInfo {
+    bool ready = false;
+    int ctas_per_sm = 0;
+};
+
+template <int D, int G>
+static bool prepare(const pkv_host::DeviceInfo &dev, int batch, int *ctas_per_sm) {
+    static std::mutex mu;
+    static LaunchInfo info[64];
+    std::lock_guard<std::mutex> lk(mu);
+    LaunchInfo &li = info[dev.device];
+    const size_t max_smem = Smem<D, G>::bytes(kMaxBatch);
+    if (!li.ready) {
+        if (max_smem > static_cast<size_t>(dev.max_smem_optin)) return false;
+        if (cudaFuncSetAttribute(decode_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(max_smem)) != cudaSuccess)
+            return false;
+        int n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel<D, G>, kThreads,
+                                                          Smem<D, G>::bytes(256)) != cudaSuccess)
+            return false;
+        li.ctas_per_sm = n < 1 ? 1 : (n > kCtasPerSm ? kCtasPerSm : n);
+        li.ready = true;
+    }
+    (void)batch;
+    *ctas_per_sm = li.ctas_per_sm;
+    return true;
+}
+
+template <int D, int G>
+static pkv_status launch(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf16 *v_cache,
+                         const int32_t *page_table, int64_t pt_stride, const int32_t *seq_lens,
+                         int B, int Hkv, int page_size, int64_t num_pages, float scale,
+                         void *workspace, int32_t *dev_status, pkv_bf16 *out,
+                         cudaStream_t stream) {
+    pkv_host::DeviceInfo dev;
+    if (!pkv_host::current_device(&dev)) return PKV_ECUDA;
+    int ctas = 0;
+    if (!prepare<D, G>(dev, B, &ctas)) return PKV_ECUDA;
+    const int T = Shape<D>::T;
+    const int box_rows = page_size < T ? page_size : T;
+    CUtensorMap kmap, vmap;
+    const int64_t slots = num_pages * page_size;
+    if (!pkv_host::encode_kv_map(&kmap, k_cache, slots, Hkv, D, D, box_rows, false) ||
+        !pkv_host::encode_kv_map(&vmap, v_cache, slots, Hkv, D, D, box_rows, false))
+        return PKV_EINVAL;
+    int ps_log2 = 0;
+    while ((1 << ps_log2) < page_size) ++ps_log2;
+    const int grid = dev.sm_count * ctas;
+    int32_t *ws_prefix = static_cast<int32_t *>(workspace);
+    float *ws_part = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) +
+                                               (((size_t)(B + 1) * 4 + 255) & ~size_t(255)));
+    const float scale_log2 = scale * kLog2e;
+    decode_kernel<D, G><<<grid, kThreads, Smem<D, G>::bytes(B), stream>>>(
+        kmap, vmap, reinterpret_cast<const __nv_bfloat16 *>(q), page_table, pt_stride, seq_lens, B,
+        Hkv, ps_log2, box_rows, num_pages, scale_log2, ws_part, ws_prefix, dev_status,
+        reinterpret_cast<__nv_bfloat16 *>(out));
+    if (cudaGetLastError() != cudaSuccess) return PKV_ECUDA;
+    decode_merge_kernel<D, G><<<B * Hkv, 128, 0, stream>>>(
+        seq_lens, ws_prefix, ws_part, B, Hkv, pt_stride * page_size, grid, dev_status,
+        reinterpret_cast<__nv_bfloat16 *>(out));
+    if (cudaGetLastError() != cudaSuccess) return PKV_ECUDA;
+    return PKV_OK;
+}
+
+}  // namespace decode
+}  // namespace pkv
+
+using namespace pkv::decode;
+
+static bool supported_gqa(int G) { return G == 1 || G == 2 || G == 4 || G == 8; }
+
+extern "C" size_t pkv_decode_workspace_size(int batch, int num_q_heads, int num_kv_heads,
+                                            int head_dim) {
+    if (batch < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads)
+        return 0;
+    if (head_dim != 64 && head_dim != 128) return 0;
+    pkv_host::DeviceInfo dev;
+    if (!pkv_host::current_device(&dev)) return 0;
+    const int G = num_q_heads / num_kv_heads;
+    const size_t grid = static_cast<size_t>(dev.sm_count) * kCtasPerSm;
+    const size_t prefix = ((static_cast<size_t>(batch) + 1) * 4 + 255) & ~size_t(255);
+    return prefix + grid * 2 * (static_cast<size_t>(G) * head_dim + 2 * G) * 4;
+}
+
+extern "C" pkv_status pkv_paged_decode_attn(const pkv_bf16 *q, const pkv_bf16 *k_cache,
+                                            const pkv_bf16 *v_cache, const int32_t *page_table,
+                                            int64_t page_table_stride, const int32_t *seq_lens,
+                                            int batch, int num_q_heads, int num_kv_heads,
+                                            int head_dim, int page_size, int64_t num_pages,
+                                            float softmax_scale, void *workspace,
+                                            size_t workspace_bytes, int32_t *dev_status,
+                                            pkv_bf16 *out, void *stream) {
+    if (batch < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_pages <= 0 ||
+        page_table_stride < 0 || page_size <= 0)
+        return PKV_EINVAL;
+    if (num_q_heads % num_kv_heads != 0) return PKV_EINVAL;
+    if (!(softmax_scale == softmax_scale)) return PKV_EINVAL;
+    if (batch == 0) return PKV_OK;
+    if (!q || !k_cache || !v_cache || !page_table || !seq_lens || !workspace || !out)
+        return PKV_EINVAL;
+    const int G = num_q_heads / num_kv_heads;
+    if ((head_dim != 64 && head_dim != 128) || !supported_gqa(G)) return PKV_EUNSUPPORTED;
+    if ((page_size & (page_size - 1)) != 0 || page_size > 256) return PKV_EUNSUPPORTED;
+    if (batch > kMaxBatch) return PKV_EUNSUPPORTED;
+    if (!pkv_host::aligned16(q) || !pkv_host::aligned16(k_cache) || !pkv_host::aligned16(v_cache) ||
+        !pkv_host::aligned16(out) || !pkv_host::aligned16(workspace))
+        return PKV_EINVAL;
+    if (num_pages * page_size > 0x7fffffffll) return PKV_EUNSUPPORTED;
+    // total tiles must fit the block's int32 prefix sums
+    const int T = head_dim == 128 ? Shape<128>::T : Shape<64>::T;
+    const int64_t max_tiles = (page_table_stride * page_size + T - 1) / T;
+    if (static_cast<double>(batch) * num_kv_heads * max_tiles >= 2147483647.0)
+        return PKV_EUNSUPPORTED;
+    if (workspace_bytes < pkv_decode_workspace_size(batch, num_q_heads, num_kv_heads, head_dim))
+        return PKV_EINVAL;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+#define PKV_DECODE_CASE(DD, GG)                                                                 \
+    if (head_dim == DD && G == GG)                                                              \
+        return launch<DD, GG>(q, k_cache, v_cache, page_table, page_table_stride, seq_lens, batch, \
+                              num_kv_heads, page_size, num_pages, softmax_scale, workspace,     \
+                              dev_status, out, st);
+    PKV_DECODE_CASE(128, 1)
+    PKV_DECODE_CASE(128, 2)
+    PKV_DECODE_CASE(128, 4)
+    PKV_DECODE_CASE(128, 8)
+    PKV_DECODE_CASE(64, 1)
+    PKV_DECODE_CASE(64, 2)
+    PKV_DECODE_CASE(64, 4)
+    PKV_DECODE_CASE(64, 8)
+#undef PKV_DECODE_CASE
+    return PKV_EUNSUPPORTED;
+}

@@ -1,0 +1,77 @@
+"""The three calls can be captured in a CUDA graph and replayed (the engines
+replay decode steps from captured graphs: miniVLLM "Engine Architecture",
+CUDA graph optimization; mini-sglang "Engine Class", CUDA Graph Optimization).
+Replays with new inputs copied into the captured buffers match the oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_out_gb300 as pkv
+from synth import make_inputs
+from tests.gpu_util import TOL, as_f64, max_err, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def _decode_inputs(seed, lens, pool_pages):
+    lens = np.asarray(lens)
+    return make_inputs(seed=seed, Hq=16, Hkv=8, d=128, page_size=16,
+                       new_lens=np.ones(len(lens), np.int64), prefix_lens=lens - 1,
+                       pool_pages=pool_pages, pt_stride=64)
+
+
+def test_decode_step_graph_replay_with_new_inputs():
+    a = _decode_inputs(60, [100, 700, 33, 1000], pool_pages=400)
+    b = _decode_inputs(61, [5, 1024, 512, 64], pool_pages=400)
+    # captured buffers
+    k, v = to_dev(a.k_cache), to_dev(a.v_cache)
+    q, kn, vn, loc = to_dev(a.q), to_dev(a.k_new), to_dev(a.v_new), to_dev(a.out_loc)
+    pt, sl = to_dev(a.page_table), to_dev(a.seq_lens)
+    out = torch.empty_like(q)
+    ws = pkv.decode_workspace(a.B, a.Hq, a.Hkv, a.d)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        # warm-up call outside the capture (first call sets kernel attributes)
+        pkv.kv_store(kn, vn, loc, k, v, dev_status=status, stream=s)
+        pkv.paged_decode_attn(q, k, v, pt, sl, a.scale, workspace=ws, dev_status=status, out=out, stream=s)
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        pkv.kv_store(kn, vn, loc, k, v, dev_status=status, stream=s)
+        pkv.paged_decode_attn(q, k, v, pt, sl, a.scale, workspace=ws, dev_status=status, out=out, stream=s)
+    for x in (a, b, a):
+        k.copy_(to_dev(x.k_cache)), v.copy_(to_dev(x.v_cache))
+        q.copy_(to_dev(x.q)), kn.copy_(to_dev(x.k_new)), vn.copy_(to_dev(x.v_new))
+        loc.copy_(to_dev(x.out_loc)), pt.copy_(to_dev(x.page_table)), sl.copy_(to_dev(x.seq_lens))
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        assert max_err(as_f64(out), oracle.run_inputs(x)) <= TOL
+
+
+def test_prefill_graph_replay():
+    x = make_inputs(seed=62, Hq=16, Hkv=8, d=128, page_size=16, new_lens=[90, 200],
+                    prefix_lens=[17, 300])
+    k, v = to_dev(x.k_cache), to_dev(x.v_cache)
+    q, kn, vn, loc = to_dev(x.q), to_dev(x.k_new), to_dev(x.v_new), to_dev(x.out_loc)
+    pt, sl, cu = to_dev(x.page_table), to_dev(x.seq_lens), to_dev(x.cu_seqlens_q)
+    out = torch.empty_like(q)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        pkv.paged_prefill_attn(q, cu, k, v, pt, sl, x.scale, x.max_q_len, dev_status=status, out=out, stream=s)
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        pkv.kv_store(kn, vn, loc, k, v, dev_status=status, stream=s)
+        pkv.paged_prefill_attn(q, cu, k, v, pt, sl, x.scale, x.max_q_len, dev_status=status, out=out, stream=s)
+    out.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert max_err(as_f64(out), oracle.run_inputs(x)) <= TOL
