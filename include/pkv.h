@@ -180,6 +180,52 @@ pkv_status pkv_paged_prefill_attn(const pkv_bf16 *q, const int32_t *cu_seqlens_q
                                   int page_size, int64_t num_pages, float softmax_scale,
                                   int32_t *dev_status, pkv_bf16 *out, void *stream);
 
+/*
+ * Size of the fixed scratch area that pkv_paged_decode_attn_noalloc uses in
+ * place of a caller-provided workspace (4 MiB, enough for head_dim 128 with
+ * 8 query heads per KV head on GPUs of up to 240 SMs).
+ */
+#define PKV_NOALLOC_SCRATCH_BYTES 4194304
+
+/*
+ * pkv_paged_decode_attn_noalloc: the same decode attention as
+ * pkv_paged_decode_attn, for callers that cannot hand the library a workspace.
+ *
+ * The pages this library follows have no counterpart of this call; it exists
+ * for callers that are not able to allocate device memory when they call
+ * attention: an inference runtime that plans every byte of device memory up
+ * front and forbids allocation on its hot path, a plugin inside another
+ * framework that is given only its inputs and outputs, or code that must not
+ * touch the allocator at all.  Instead of a workspace argument, the call uses
+ * one scratch array of PKV_NOALLOC_SCRATCH_BYTES that the library declares in
+ * device memory; every GPU that loads the library holds that array until the
+ * process exits.  The call itself never allocates or frees memory (no
+ * cudaMalloc, cudaFree or allocating library routine).
+ *
+ *   - Arguments, layouts, results and device error bits are those of
+ *     pkv_paged_decode_attn without workspace / workspace_bytes.
+ *   - Sizes whose workspace (pkv_decode_workspace_size) would exceed
+ *     PKV_NOALLOC_SCRATCH_BYTES are rejected with PKV_EUNSUPPORTED and nothing
+ *     is launched.
+ *   - The first call on each device looks up the device address of the
+ *     scratch array for that device (a host-side query, made once per device
+ *     with that device current).  Make that first call before any stream
+ *     capture.
+ *   - All calls share the one scratch array and it keeps whatever the last
+ *     call left there; the kernels write every scratch word they read, so
+ *     nothing needs clearing between calls.  Two calls whose kernels overlap
+ *     on the GPU (different streams, no ordering between them) race on the
+ *     scratch array and may return wrong results: order them on one stream or
+ *     with events.
+ */
+pkv_status pkv_paged_decode_attn_noalloc(const pkv_bf16 *q, const pkv_bf16 *k_cache,
+                                         const pkv_bf16 *v_cache, const int32_t *page_table,
+                                         int64_t page_table_stride, const int32_t *seq_lens,
+                                         int batch, int num_q_heads, int num_kv_heads,
+                                         int head_dim, int page_size, int64_t num_pages,
+                                         float softmax_scale, int32_t *dev_status,
+                                         pkv_bf16 *out, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

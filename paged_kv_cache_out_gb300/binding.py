@@ -33,6 +33,8 @@ SIGNATURES = {
                                _F32, _P, _SZ, _P, _P, _P], _I32),
     "pkv_paged_prefill_attn": ([_P, _P, _P, _P, _P, _I64, _P, _I32, _I64, _I32, _I32, _I32,
                                 _I32, _I32, _I64, _F32, _P, _P, _P], _I32),
+    "pkv_paged_decode_attn_noalloc": ([_P, _P, _P, _P, _I64, _P, _I32, _I32, _I32, _I32, _I32,
+                                       _I64, _F32, _P, _P, _P], _I32),
 }
 
 
