@@ -177,6 +177,10 @@ def to_dev(a, dev):
     return t.to(dev)
 
 
+def batch_override(args):
+    return {"B": args.batch} if args.batch else {}
+
+
 def run_gpu(args, rank, world):
     import torch
     import paged_kv_cache_out_gb300 as pkv
@@ -187,7 +191,7 @@ def run_gpu(args, rank, world):
     pkv.load_library()
     hbm_peak, bf16_peak, bf16_sus, peak_kind = measured_peaks()
 
-    x = make_config(args.workload, seed=args.seed + rank)
+    x = make_config(args.workload, seed=args.seed + rank, **batch_override(args))
     assert x.meta["phase"] == "decode", "the GPU arm times a decode workload"
     stream = torch.cuda.Stream(device=dev)
     k, v = to_dev(x.k_cache, dev), to_dev(x.v_cache, dev)
@@ -408,7 +412,7 @@ def run_reference(args):
     import oracle
     from synth import make_config
     oracle.build()
-    x = make_config(args.workload, seed=args.seed)
+    x = make_config(args.workload, seed=args.seed, **batch_override(args))
     threads = oracle.max_threads()
     per_step = max(1.0, 20.0 / max(1, args.steps + args.warmup))
     for _ in range(args.warmup):
@@ -443,6 +447,8 @@ def main():
     ap.add_argument("--workload", default="qwen3_decode",
                     choices=["tiny_decode", "qwen3_decode", "llama_long_decode"])
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--batch", type=int, default=0,
+                    help="number of sequences of the decode workload (default: the workload's own)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -461,7 +467,8 @@ def main():
     if rank == 0:
         if not args.no_cpu_baseline:
             from synth import make_config
-            line["cpu_baseline"] = cpu_baseline(make_config(args.workload, seed=args.seed))
+            line["cpu_baseline"] = cpu_baseline(make_config(args.workload, seed=args.seed,
+                                                            **batch_override(args)))
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
