@@ -9,6 +9,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "pkv.h"
 
 namespace pkv {
@@ -86,6 +88,20 @@ __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, vo
     return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort, dev_status));
 }
 
+// ---------------------------------------------------------------- dependent launch
+// Programmatic dependent launch: a kernel launched with launch_dependent()
+// may become resident while the kernel before it in the stream is still
+// running; it must execute grid_dependency_wait() before it reads anything an
+// earlier kernel wrote (the wait returns once those kernels have completed
+// and their memory is visible).  allow_dependents() lets the next kernel in
+// the stream be scheduled early.
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void allow_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- barriers
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
@@ -139,6 +155,23 @@ __device__ __forceinline__ float ex2(float x) {  // 2^x on the SFU
     return y;
 }
 
+// 2^x on the FMA pipe, for x in [-125, 126]: x = j + f with j = round(x) (the
+// 1.5 * 2^23 addition leaves round(x) in the low mantissa bits) and
+// f in [-1/2, 1/2]; 2^f by a cubic fitted here to 2^f on [-1/2, 1/2]
+// (Chebyshev-node least squares, reweighted towards minimax relative error:
+// max relative error 7.5e-5 in fp32); 2^j is added to the exponent field.
+// Used for part of the softmax exponentials so the SFU is not the only unit
+// computing them.
+__device__ __forceinline__ float exp2_poly(float x) {
+    const float t = x + 12582912.0f;
+    const int j = __float_as_int(t) - 0x4B400000;
+    const float f = x - (t - 12582912.0f);
+    float p = fmaf(0.0551716648042202f, f, 0.2426111251115799f);
+    p = fmaf(p, f, 0.6932609677314758f);
+    p = fmaf(p, f, 0.9999280571937561f);
+    return __int_as_float(__float_as_int(p) + (j << 23));
+}
+
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
@@ -184,6 +217,16 @@ __device__ __forceinline__ void umma_bf16_ss(uint32_t d_tmem, uint64_t a_desc, u
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
+// D[tmem] (+)= A[tmem] * B[smem]^T, kind::f16: A (bf16, two per 32-bit column,
+// row m in TMEM lane m) is read from tensor memory.
+__device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                             uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
 // Arrive on `bar` once every tcgen05.mma this thread issued before has completed.
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
     asm volatile(
@@ -209,6 +252,15 @@ __device__ __forceinline__ void tmem_ld_32cols(uint32_t taddr, uint32_t *r) {
           "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
           "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
         : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_st_16cols(uint32_t taddr, const uint32_t *r) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+        "r"(r[15])
+        : "memory");
 }
 __device__ __forceinline__ void tmem_st_32cols(uint32_t taddr, const uint32_t *r) {
     asm volatile(
@@ -251,5 +303,23 @@ bool encode_q_map(CUtensorMap *map, const void *base, int64_t tokens, int num_q_
                   int head_dim, int box_heads, int box_tokens);
 
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Launch `kernel` on `stream` as a programmatic dependent of the work before
+// it (see grid_dependency_wait on the device side).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                    cudaStream_t stream, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 }  // namespace pkv_host

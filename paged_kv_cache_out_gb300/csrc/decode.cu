@@ -62,8 +62,9 @@ struct Smem {
     static constexpr int BARS = 2 * S::STAGES * 8;
     static constexpr int FLAGS = S::STAGES * 4 + 16;
     static constexpr int FIXED = RING + RED_O + RED_ML + BARS + FLAGS;
+    // + tile offsets [batch + 1] and sequence lengths [batch], int32
     static size_t bytes(int batch) {
-        return 1024 /* alignment slack */ + FIXED + static_cast<size_t>(batch + 1) * 4;
+        return 1024 /* alignment slack */ + FIXED + static_cast<size_t>(2 * batch + 1) * 4;
     }
 };
 
@@ -116,15 +117,21 @@ __device__ __forceinline__ bool next_piece(int64_t &pos, int64_t end, int64_t bl
     return true;
 }
 
-// Block-wide exclusive scan: prefix[b] = Hkv * sum_{b' < b} ntiles(b').
-__device__ void build_prefix(int32_t *prefix, const int32_t *seq_lens, int B, int Hkv,
-                             int64_t cap, int T, int32_t *scratch /* kThreads/32 + 1 ints */) {
+// Block-wide exclusive scan: prefix[b] = Hkv * sum_{b' < b} ntiles(b'); the
+// lengths themselves are kept in lens[b].
+__device__ void build_prefix(int32_t *prefix, int32_t *lens, const int32_t *seq_lens, int B,
+                             int Hkv, int64_t cap, int T,
+                             int32_t *scratch /* kThreads/32 + 1 ints */) {
     const int tid = threadIdx.x;
     const int per = (B + kThreads - 1) / kThreads;
     const int lo = tid * per;
     const int hi = min(B, lo + per);
     int local = 0;
-    for (int b = lo; b < hi; ++b) local += ntiles_of(seq_lens[b], cap, T) * Hkv;
+    for (int b = lo; b < hi; ++b) {
+        const int L = seq_lens[b];
+        lens[b] = L;
+        local += ntiles_of(L, cap, T) * Hkv;
+    }
     // inclusive scan of `local` over the block
     const int lane = tid & 31, warp = tid >> 5;
     int v = local;
@@ -148,7 +155,7 @@ __device__ void build_prefix(int32_t *prefix, const int32_t *seq_lens, int B, in
     int run = scratch[warp] + v - local;  // exclusive prefix of this thread's chunk
     for (int b = lo; b < hi; ++b) {
         prefix[b] = run;
-        run += ntiles_of(seq_lens[b], cap, T) * Hkv;
+        run += ntiles_of(lens[b], cap, T) * Hkv;
     }
     if (tid == 0) prefix[B] = scratch[kThreads / 32];
     __syncthreads();
@@ -178,8 +185,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     int *flags = reinterpret_cast<int *>(smem + M::RING + M::RED_O + M::RED_ML + M::BARS);
     volatile int *abort_flag = flags + STAGES;
     int32_t *prefix = reinterpret_cast<int32_t *>(smem + M::FIXED);
+    int32_t *lens = prefix + (B + 1);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    grid_dependency_wait();  // the pool rows of this step are written by the kernel before
+    allow_dependents();      // the merge kernel may become resident and wait for us
     if (tid == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(smem_u32(&bars[s]), 1);                        // full: producer + tx bytes
@@ -189,7 +199,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_mbar_init();
     }
     // red_ml doubles as the scan scratch before any piece is reduced
-    build_prefix(prefix, seq_lens, B, Hkv, cap, T, reinterpret_cast<int32_t *>(red_ml));
+    build_prefix(prefix, lens, seq_lens, B, Hkv, cap, T, reinterpret_cast<int32_t *>(red_ml));
     if (blockIdx.x == 0)
         for (int b = tid; b <= B; b += kThreads) ws_prefix[b] = prefix[b];
 
@@ -212,14 +222,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         Piece p;
         uint32_t it = 0;
         bool ok = true;
+        // boxes per tile; up to 32 of them page ids come in warp-wide windows
+        // of 32 boxes, the next window loaded one window ahead
+        const int bpt = T / box_rows;
         while (ok && next_piece(pos, my_end, my_start, prefix, B, Hkv, p)) {
-            const int L = seq_lens[p.b];
+            const int L = lens[p.b];
             const int32_t *prow = page_table + (int64_t)p.b * pt_stride;
+            auto load_window = [&](int w) -> int {
+                const int key = (32 * w + lane) * box_rows;
+                return key < L ? prow[key >> ps_log2] : 0;
+            };
+            int w_cur = (p.t0 * bpt) >> 5;
+            int pg_cur = 0, pg_nxt = 0;
+            if (bpt <= 32) {
+                pg_cur = load_window(w_cur);
+                pg_nxt = load_window(w_cur + 1);
+            }
             for (int tile = p.t0; tile < p.t1; ++tile, ++it) {
                 const int s = it % STAGES;
                 const uint32_t ph = (it / STAGES) & 1;
                 if (it >= STAGES && !mbar_wait_warp(smem_u32(&bars[STAGES + s]), ph ^ 1, abort_flag,
-                                               dev_status)) {
+                                                    dev_status)) {
                     ok = false;
                     break;
                 }
@@ -229,12 +252,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // page ids of this tile's boxes (at most T boxes: two per lane)
                 int pg[2] = {0, 0};
                 bool bad = false;
+                if (bpt <= 32) {
+                    const int b0 = tile * bpt;
+                    if ((b0 >> 5) != w_cur) {
+                        w_cur = b0 >> 5;
+                        pg_cur = pg_nxt;
+                        pg_nxt = load_window(w_cur + 1);
+                    }
+                    pg[0] = __shfl_sync(0xffffffffu, pg_cur, (b0 + (lane % bpt)) & 31);
+                    if (lane < nbox && (pg[0] < 0 || pg[0] >= num_pages)) bad = true;
+                } else {
 #pragma unroll
-                for (int k = 0; k < 2; ++k) {
-                    const int i = lane + 32 * k;
-                    if (i < nbox) {
-                        pg[k] = prow[(tok0 + i * box_rows) >> ps_log2];
-                        if (pg[k] < 0 || pg[k] >= num_pages) bad = true;
+                    for (int k = 0; k < 2; ++k) {
+                        const int i = lane + 32 * k;
+                        if (i < nbox) {
+                            pg[k] = prow[(tok0 + i * box_rows) >> ps_log2];
+                            if (pg[k] < 0 || pg[k] >= num_pages) bad = true;
+                        }
                     }
                 }
                 bad = __any_sync(0xffffffffu, bad);
@@ -281,7 +315,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t it = 0;
     bool ok = true;
     while (ok && next_piece(pos, my_end, my_start, prefix, B, Hkv, p)) {
-        const int L = seq_lens[p.b];
+        const int L = lens[p.b];
 #pragma unroll
         for (int h = 0; h < G; ++h) {
             m[h] = kNegBig;
@@ -437,6 +471,7 @@ __global__ void __launch_bounds__(128)
                         const float *__restrict__ ws_part, int B, int Hkv, int64_t cap, int grid,
                         int32_t *dev_status, __nv_bfloat16 *__restrict__ out) {
     using S = Shape<D>;
+    grid_dependency_wait();  // partial states come from the main kernel
     const int b = blockIdx.x / Hkv, g = blockIdx.x % Hkv;
     const int Hq = Hkv * G;
     __nv_bfloat16 *orow = out + ((int64_t)b * Hq + (int64_t)g * G) * D;
@@ -535,15 +570,19 @@ static pkv_status launch(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_b
     float *ws_part = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) +
                                                (((size_t)(B + 1) * 4 + 255) & ~size_t(255)));
     const float scale_log2 = scale * kLog2e;
-    decode_kernel<D, G><<<grid, kThreads, Smem<D, G>::bytes(B), stream>>>(
-        kmap, vmap, reinterpret_cast<const __nv_bfloat16 *>(q), page_table, pt_stride, seq_lens, B,
-        Hkv, ps_log2, box_rows, num_pages, scale_log2, ws_part, ws_prefix, dev_status,
-        reinterpret_cast<__nv_bfloat16 *>(out));
-    if (cudaGetLastError() != cudaSuccess) return PKV_ECUDA;
-    decode_merge_kernel<D, G><<<B * Hkv, 128, 0, stream>>>(
-        seq_lens, ws_prefix, ws_part, B, Hkv, pt_stride * page_size, grid, dev_status,
-        reinterpret_cast<__nv_bfloat16 *>(out));
-    if (cudaGetLastError() != cudaSuccess) return PKV_ECUDA;
+    if (pkv_host::launch_dependent(decode_kernel<D, G>, dim3(grid), dim3(kThreads),
+                                   Smem<D, G>::bytes(B), stream, kmap, vmap,
+                                   reinterpret_cast<const __nv_bfloat16 *>(q), page_table, pt_stride,
+                                   seq_lens, B, Hkv, ps_log2, box_rows, num_pages, scale_log2,
+                                   ws_part, ws_prefix, dev_status,
+                                   reinterpret_cast<__nv_bfloat16 *>(out)) != cudaSuccess)
+        return PKV_ECUDA;
+    if (pkv_host::launch_dependent(decode_merge_kernel<D, G>, dim3(B * Hkv), dim3(128), 0, stream,
+                                   seq_lens, static_cast<const int32_t *>(ws_prefix),
+                                   static_cast<const float *>(ws_part), B, Hkv,
+                                   pt_stride * page_size, grid, dev_status,
+                                   reinterpret_cast<__nv_bfloat16 *>(out)) != cudaSuccess)
+        return PKV_ECUDA;
     return PKV_OK;
 }
 

@@ -17,6 +17,8 @@ __global__ void __launch_bounds__(kStoreThreads) kv_store_kernel(
     const uint4 *__restrict__ k_new, const uint4 *__restrict__ v_new,
     const int32_t *__restrict__ out_loc, int64_t num_tokens, uint4 *__restrict__ k_cache,
     uint4 *__restrict__ v_cache, int64_t num_slots, int row_vecs, int32_t *dev_status) {
+    grid_dependency_wait();  // inputs may come from the kernel before this one
+    allow_dependents();
     const int lane = threadIdx.x & 31;
     const int64_t warp = (static_cast<int64_t>(blockIdx.x) * kStoreThreads + threadIdx.x) >> 5;
     const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * kStoreThreads) >> 5;
@@ -70,9 +72,11 @@ extern "C" pkv_status pkv_kv_store(const pkv_bf16 *k_new, const pkv_bf16 *v_new,
         (warps_needed + pkv::kStoreThreads / 32 - 1) / (pkv::kStoreThreads / 32);
     const int64_t max_blocks = static_cast<int64_t>(dev.sm_count) * 8;
     const int blocks = static_cast<int>(blocks_needed < max_blocks ? blocks_needed : max_blocks);
-    pkv::kv_store_kernel<<<blocks, pkv::kStoreThreads, 0, static_cast<cudaStream_t>(stream)>>>(
-        reinterpret_cast<const uint4 *>(k_new), reinterpret_cast<const uint4 *>(v_new), out_loc,
-        num_tokens, reinterpret_cast<uint4 *>(k_cache), reinterpret_cast<uint4 *>(v_cache),
+    const cudaError_t err = pkv_host::launch_dependent(
+        pkv::kv_store_kernel, dim3(blocks), dim3(pkv::kStoreThreads), 0,
+        static_cast<cudaStream_t>(stream), reinterpret_cast<const uint4 *>(k_new),
+        reinterpret_cast<const uint4 *>(v_new), out_loc, num_tokens,
+        reinterpret_cast<uint4 *>(k_cache), reinterpret_cast<uint4 *>(v_cache),
         num_pages * page_size, row_vecs, dev_status);
-    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ECUDA;
+    return err == cudaSuccess ? PKV_OK : PKV_ECUDA;
 }

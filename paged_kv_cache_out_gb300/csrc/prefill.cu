@@ -9,28 +9,37 @@
 // 0 .. c_r + i (causal, aligned at the bottom right).  Grouped-query
 // attention shares one KV head among num_q_heads / num_kv_heads query heads.
 //
-// One block computes a 128-row tile of (token, query head) rows of one
-// request and one KV head: 128/G consecutive new tokens x the G query heads of
-// that KV head, so every K/V tile staged in shared memory serves all G heads.
-// Roles (256 threads):
-//   warp 0      producer: Q once, then 128-key K and V tiles through a
-//               2-stage ring.  Pages of >= 8 tokens come in as TMA boxes
-//               (one per page, 128-byte swizzle, straight into the layout the
-//               tensor core reads); smaller pages are gathered by the warp's
-//               lanes with 16-byte loads and swizzled stores.
-//   warp 1      allocates 512 TMEM columns (two 128x128 fp32 score buffers and
-//               the 128 x head_dim fp32 output accumulator); one lane issues
-//               S = Q K^T (M=128, N=128, K=head_dim) and O += P V (M=128,
-//               N=head_dim, K=128), bf16 operands from shared memory.
-//   warps 4-7   softmax: thread i owns row i (TMEM lane i): reads its scores,
-//               applies the causal mask by selection, keeps a running max and
-//               sum in the log2 domain, writes P as bf16 into shared memory in
-//               the swizzled K-major layout, and rescales the TMEM output row
-//               when the running max grew by more than 2^8; at the end it
-//               normalises the output row and stores it.
-//   warps 2-3   idle.
-// QK^T of tile j+1 and PV of tile j-1 run on the tensor cores while the
-// softmax warps compute the exponentials of tile j.
+// One block (one per SM) owns two 128-row query tiles, A and B, of one
+// request and one KV head; a tile holds 128/G consecutive new tokens x the G
+// query heads of that KV head, so every K/V tile staged in shared memory
+// serves 2 x 128 rows.  Roles (320 threads):
+//   warp 8      producer: Q tiles A and B once, then 128-key K and V tiles
+//               through 2-stage rings, K one tile ahead of V.  Pages of >= 8 tokens come in as TMA
+//               boxes (one per page and 64-column block, 128-byte swizzle,
+//               straight into the layout the tensor core reads); smaller
+//               pages are gathered by the warp's lanes with 16-byte loads and
+//               swizzled stores.  Page ids are read in warp-wide windows, one
+//               window ahead.
+//   warp 9      allocates all 512 TMEM columns (per query tile: a 128x128 fp32
+//               score buffer S, whose first 64 columns then hold P as bf16
+//               pairs, and a 128 x head_dim fp32 output accumulator O); one
+//               lane issues, in this order per key tile j,
+//                 O_A += P_A(j) V_j,  S_A(j+1) = Q_A K_(j+1)^T,
+//                 O_B += P_B(j) V_j,  S_B(j+1) = Q_B K_(j+1)^T,
+//               with S from Q and K in shared memory (M=128, N=128,
+//               K=head_dim) and PV reading P from tensor memory and V from
+//               shared memory (M=128, N=head_dim, K=128).  Because the tensor
+//               core runs one block's MMAs in order, the commit of S(j+1) also
+//               tells that PV(j) has read P(j) and written O.
+//   warps 0-3   softmax of tile A, warps 4-7 softmax of tile B: thread i of a
+//               warpgroup owns row i (TMEM lane i): reads its scores, applies
+//               the causal mask by selection, keeps a running max and sum in
+//               the log2 domain, rescales its TMEM output row when the running
+//               max grew by more than 2^8 (exact: every term shares the
+//               reference), writes P into tensor memory, and at the end
+//               normalises and stores the row.
+// While one tile's softmax runs, the tensor core works on the other tile's PV
+// and QK^T.
 #include <math.h>
 
 #include <mutex>
@@ -40,10 +49,12 @@
 namespace pkv {
 namespace prefill {
 
-constexpr int kThreads = 256;
-constexpr int BM = 128;  // rows of a tile: (token, head) pairs
+constexpr int kThreads = 320;
+constexpr int BM = 128;  // rows of a query tile: (token, head) pairs
+constexpr int NQ = 2;    // query tiles per block
 constexpr int BN = 128;  // keys per KV tile
-constexpr int kStages = 2;
+constexpr int kKStages = 2, kVStages = 2;
+constexpr int kProducerWarp = 8, kMmaWarp = 9;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kNegBig = -1.0e30f;
 constexpr float kRescaleLog2 = 8.0f;  // lazy rescale threshold (factor 256)
@@ -51,21 +62,20 @@ constexpr uint32_t kTmemCols = 512;
 
 template <int D>
 struct Layout {
-    static constexpr int BLK = BM * 128;             // one 64-column swizzled block, 128 rows
-    static constexpr int Q_BYTES = (D / 64) * BLK;   // Q tile
-    static constexpr int KV_BYTES = (D / 64) * BLK;  // one K or V tile (128 keys)
-    static constexpr int P_BYTES = (BN / 64) * BLK;  // P tile, 128 x 128 bf16
+    static constexpr int BLK = BM * 128;              // one 64-column swizzled block, 128 rows
+    static constexpr int KBLK = BN * 128;             // one 64-column block of a K/V tile
+    static constexpr int Q_BYTES = (D / 64) * BLK;    // one query tile
+    static constexpr int KV_BYTES = (D / 64) * KBLK;  // one K or V tile (128 keys)
     static constexpr int OFF_Q = 0;
-    static constexpr int OFF_K = OFF_Q + Q_BYTES;
-    static constexpr int OFF_V = OFF_K + kStages * KV_BYTES;
-    static constexpr int OFF_P = OFF_V + kStages * KV_BYTES;
-    static constexpr int OFF_BAR = OFF_P + P_BYTES;
-    // barriers: q_full, kfull[2], kempty[2], vfull[2], vempty[2], sfull[2], sfree[2], pfull, odone
-    static constexpr int NBARS = 1 + 4 * kStages + 2 + 2 + 2;
+    static constexpr int OFF_K = OFF_Q + NQ * Q_BYTES;
+    static constexpr int OFF_V = OFF_K + kKStages * KV_BYTES;
+    static constexpr int OFF_BAR = OFF_V + kVStages * KV_BYTES;
+    // qfull, kfull/kempty[kKStages], vfull/vempty[kVStages], per query tile: sfull, pfull, odone
+    static constexpr int NBARS = 1 + 2 * kKStages + 2 * kVStages + NQ * 3;
     static constexpr int OFF_MISC = OFF_BAR + NBARS * 8;
     static constexpr int TOTAL = OFF_MISC + 64;
-    // at least 116 KB so that two blocks never share an SM: each holds 512 TMEM columns
-    static constexpr size_t bytes() { return (1024 + TOTAL) > 118784 ? (1024 + TOTAL) : 118784; }
+    // at least 116 KB: one block per SM (it holds all 512 TMEM columns)
+    static constexpr size_t bytes() { return TOTAL > 118784 ? TOTAL : 118784; }
 };
 
 // tcgen05 shared-memory matrix descriptor: 128-byte swizzle, fixed version 1.
@@ -85,10 +95,9 @@ __host__ __device__ constexpr uint32_t instr_desc(int M, int N, bool b_mn_major)
            (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
-// Byte offset of element (row, col) of a [rows x 64k] bf16 tile stored as
-// 64-column blocks of `rows` x 128 B with the 128-byte swizzle.
-__device__ __forceinline__ uint32_t swz_offset(int row, int chunk16 /* 16-byte column chunk */,
-                                               int rows) {
+// Byte offset of 16-byte column chunk `chunk16` of row `row` in a tile stored
+// as 64-column blocks of `rows` x 128 B with the 128-byte swizzle.
+__device__ __forceinline__ uint32_t swz_offset(int row, int chunk16, int rows) {
     const int blk = chunk16 >> 3, c = chunk16 & 7;
     return static_cast<uint32_t>(blk * rows * 128 + row * 128 + ((c ^ (row & 7)) << 4));
 }
@@ -103,11 +112,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                    int ps_log2, int box_rows, int64_t num_pages, float scale_log2, int mtiles,
                    int32_t *dev_status, __nv_bfloat16 *__restrict__ out) {
     using Lo = Layout<D>;
-    constexpr int TOK = BM / G;  // new tokens per tile
+    constexpr int TOK = BM / G;  // new tokens per query tile
     const int Hq = Hkv * G;
     const int64_t cap = pt_stride << ps_log2;
 
-    // ---- which tile: heaviest (largest mt) first over all requests and heads
+    // ---- which tiles: heaviest (largest mt) first over all requests and heads
     const int lin = blockIdx.x;
     const int per_mt = B * Hkv;
     const int mt = mtiles - 1 - lin / per_mt;
@@ -124,40 +133,47 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (tid == 0 && mt == 0 && g == 0 && dev_status) atomicOr(dev_status, PKV_DEV_BAD_CUSEQ);
         return;
     }
-    const int tok_begin = mt * TOK;
-    if (tok_begin >= n) return;
-    const int tok_end = min(n, tok_begin + TOK);
+    const int blk_tok0 = mt * NQ * TOK;
+    if (blk_tok0 >= n) return;
+    const int blk_tok1 = min(n, blk_tok0 + NQ * TOK);
     const bool len_bad = (c < 0) || (L > cap);
     if (len_bad) {
         if (tid == 0 && mt == 0 && g == 0 && dev_status) atomicOr(dev_status, PKV_DEV_BAD_SEQLEN);
-        // rows are known: write NaN
-        for (int idx = tid; idx < (tok_end - tok_begin) * G * D; idx += kThreads) {
-            const int t = tok_begin + idx / (G * D);
+        for (int idx = tid; idx < (blk_tok1 - blk_tok0) * G * D; idx += kThreads) {
+            const int t = blk_tok0 + idx / (G * D);
             const int rem = idx % (G * D);
             out[((int64_t)(cu0 + t) * Hq + (int64_t)g * G) * D + rem] =
                 __float2bfloat16_rn(__int_as_float(0x7fc00000));
         }
         return;
     }
-    const int kend = c + tok_end;  // keys [0, kend) are needed by this tile
-    const int n_kt = (kend + BN - 1) / BN;
+    // per query tile: token range and number of 128-key tiles it needs
+    int tbeg[NQ], tend[NQ], nkt[NQ];
+#pragma unroll
+    for (int qt = 0; qt < NQ; ++qt) {
+        tbeg[qt] = blk_tok0 + qt * TOK;
+        tend[qt] = min(n, tbeg[qt] + TOK);
+        nkt[qt] = tend[qt] > tbeg[qt] ? (c + tend[qt] + BN - 1) / BN : 0;
+    }
+    const int n_kt = nkt[0] > nkt[1] ? nkt[0] : nkt[1];
 
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                                ~uintptr_t(1023));
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Lo::OFF_BAR);
-    const uint32_t bar0 = smem_u32(bars);
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = smem_raw;
+    if (smem_u32(smem) & 1023u) {  // the 128-byte swizzle needs 1024-byte aligned tiles
+        if (tid == 0 && dev_status) atomicOr(dev_status, PKV_DEV_TIMEOUT);
+        return;
+    }
+    const uint32_t bar0 = smem_u32(smem + Lo::OFF_BAR);
     auto BAR = [&](int i) -> uint32_t { return bar0 + 8u * i; };
-    // barrier indices
     const int B_QFULL = 0;
     auto B_KFULL = [](int s) { return 1 + s; };
-    auto B_KEMPTY = [](int s) { return 1 + kStages + s; };
-    auto B_VFULL = [](int s) { return 1 + 2 * kStages + s; };
-    auto B_VEMPTY = [](int s) { return 1 + 3 * kStages + s; };
-    auto B_SFULL = [](int b) { return 1 + 4 * kStages + b; };
-    auto B_SFREE = [](int b) { return 3 + 4 * kStages + b; };
-    const int B_PFULL = 5 + 4 * kStages;
-    const int B_ODONE = 6 + 4 * kStages;
+    auto B_KEMPTY = [](int s) { return 1 + kKStages + s; };
+    auto B_VFULL = [](int s) { return 1 + 2 * kKStages + s; };
+    auto B_VEMPTY = [](int s) { return 1 + 2 * kKStages + kVStages + s; };
+    constexpr int kTileBar0 = 1 + 2 * kKStages + 2 * kVStages;
+    auto B_SFULL = [](int qt) { return kTileBar0 + qt * 3; };
+    auto B_PFULL = [](int qt) { return kTileBar0 + qt * 3 + 1; };
+    auto B_ODONE = [](int qt) { return kTileBar0 + qt * 3 + 2; };
     volatile int *misc = reinterpret_cast<volatile int *>(smem + Lo::OFF_MISC);
     volatile int *abort_flag = misc + 0;
     volatile int *bad_page = misc + 1;
@@ -165,23 +181,24 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (tid == 0) {
         mbar_init(BAR(B_QFULL), 1);
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < kKStages; ++s) {
             mbar_init(BAR(B_KFULL(s)), 1);
             mbar_init(BAR(B_KEMPTY(s)), 1);
+        }
+        for (int s = 0; s < kVStages; ++s) {
             mbar_init(BAR(B_VFULL(s)), 1);
             mbar_init(BAR(B_VEMPTY(s)), 1);
         }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(BAR(B_SFULL(b)), 1);
-            mbar_init(BAR(B_SFREE(b)), 4);
+        for (int qt = 0; qt < NQ; ++qt) {
+            mbar_init(BAR(B_SFULL(qt)), 1);
+            mbar_init(BAR(B_PFULL(qt)), 4);
+            mbar_init(BAR(B_ODONE(qt)), 1);
         }
-        mbar_init(BAR(B_PFULL), 4);
-        mbar_init(BAR(B_ODONE), 1);
         *abort_flag = 0;
         *bad_page = 0;
         fence_mbar_init();
     }
-    if (warp == 1) {
+    if (warp == kMmaWarp) {
         tmem_alloc(smem_u32(tmem_slot), kTmemCols);
         tmem_relinquish();
     }
@@ -189,134 +206,172 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t tm_s[2] = {tmem, tmem + 128};
-    const uint32_t tm_o = tmem + 256;
+    // TMEM columns: S (then P over its first 64 columns) of tile qt at 128 qt,
+    // O of tile qt at 256 + 128 qt
+    auto tm_s = [&](int qt) -> uint32_t { return tmem + qt * BN; };
+    auto tm_o = [&](int qt) -> uint32_t { return tmem + NQ * BN + qt * 128; };
 
     const uint32_t sQ = smem_u32(smem + Lo::OFF_Q);
     const uint32_t sK = smem_u32(smem + Lo::OFF_K);
     const uint32_t sV = smem_u32(smem + Lo::OFF_V);
-    const uint32_t sP = smem_u32(smem + Lo::OFF_P);
     const int32_t *prow = page_table + (int64_t)r * pt_stride;
 
-    if (warp == 0) {
+    if (warp == kProducerWarp) {
         // ================================================================ producer
-        const uint64_t pol_kv = l2_evict_last_policy();  // K/V tiles are re-read by other tiles
+        const uint64_t pol_kv = l2_evict_last_policy();  // K/V tiles are re-read by other blocks
         if (lane == 0) {
             prefetch_tmap(&qmap);
             if (box_rows >= 8) {
                 prefetch_tmap(&kmap);
                 prefetch_tmap(&vmap);
             }
-            mbar_arrive_expect_tx(BAR(B_QFULL), static_cast<uint32_t>(Lo::Q_BYTES));
+            mbar_arrive_expect_tx(BAR(B_QFULL), static_cast<uint32_t>(NQ * Lo::Q_BYTES));
+            const uint64_t pol_q = l2_evict_first_policy();
 #pragma unroll
-            for (int blk = 0; blk < D / 64; ++blk)
-                tma_load_3d(sQ + blk * Lo::BLK, &qmap, BAR(B_QFULL), blk * 64, g * G,
-                            cu0 + tok_begin, l2_evict_first_policy());
+            for (int qt = 0; qt < NQ; ++qt)
+#pragma unroll
+                for (int blk = 0; blk < D / 64; ++blk)
+                    tma_load_3d(sQ + qt * Lo::Q_BYTES + blk * Lo::BLK, &qmap, BAR(B_QFULL), blk * 64,
+                                g * G, cu0 + tbeg[qt], pol_q);
         }
         const int ps_mask = (1 << ps_log2) - 1;
-        bool ok = true;
-        for (int j = 0; ok && j < n_kt; ++j) {
-            const int s = j % kStages;
-            const uint32_t ph = (j / kStages) & 1;
+        // page ids in warp-wide windows of 32 boxes, the next window loaded ahead
+        const int bpt = box_rows >= 8 ? BN / box_rows : 1;  // boxes per tile (<= 16)
+        auto load_window = [&](int w) -> int {
+            const int key = (32 * w + lane) * box_rows;
+            return (box_rows >= 8 && key < L) ? prow[key >> ps_log2] : 0;
+        };
+        int w_cur = 0;
+        int pg_cur = load_window(0), pg_nxt = load_window(1);
+        // one K or V tile: wait for its slot, then TMA boxes (or gather)
+        auto load_tile = [&](int kv, int j, int pg_tile) -> bool {
+            const int ns = kv ? kVStages : kKStages;
+            const int s = j % ns;
+            const uint32_t ph = (j / ns) & 1;
+            const uint32_t full = BAR(kv ? B_VFULL(s) : B_KFULL(s));
+            const uint32_t empty = BAR(kv ? B_VEMPTY(s) : B_KEMPTY(s));
+            const uint32_t dst = (kv ? sV : sK) + s * Lo::KV_BYTES;
             const int key0 = j * BN;
             const int nkeys = min(BN, L - key0);  // keys of this tile that exist in pages
-            for (int kv = 0; ok && kv < 2; ++kv) {
-                const uint32_t full = BAR(kv ? B_VFULL(s) : B_KFULL(s));
-                const uint32_t empty = BAR(kv ? B_VEMPTY(s) : B_KEMPTY(s));
-                const uint32_t dst = (kv ? sV : sK) + s * Lo::KV_BYTES;
-                if (j >= kStages && !mbar_wait_warp(empty, ph ^ 1, abort_flag, dev_status)) {
-                    ok = false;
-                    break;
+            if (j >= ns && !mbar_wait_warp(empty, ph ^ 1, abort_flag, dev_status)) return false;
+            if (box_rows >= 8) {
+                const int nbox = (nkeys + box_rows - 1) / box_rows;  // <= 16
+                const bool bad = lane < nbox && (pg_tile < 0 || pg_tile >= num_pages);
+                const int nbad = __popc(__ballot_sync(0xffffffffu, bad));
+                if (lane == 0) {
+                    if (nbad) *bad_page = 1;
+                    mbar_arrive_expect_tx(
+                        full, static_cast<uint32_t>((nbox - nbad) * (D / 64) * box_rows * 128));
                 }
-                if (box_rows >= 8) {
-                    // one TMA box per page (or per 128-key slice of a large page) and 64-column block
-                    const int nbox = (nkeys + box_rows - 1) / box_rows;  // <= 16
-                    int pg = 0;
-                    bool bad = false;
-                    if (lane < nbox) {
-                        pg = prow[(key0 + lane * box_rows) >> ps_log2];
-                        bad = (pg < 0 || pg >= num_pages);
-                    }
-                    const unsigned badmask = __ballot_sync(0xffffffffu, bad);
-                    const int nbad = __popc(badmask);
-                    if (lane == 0) {
-                        if (nbad) *bad_page = 1;
-                        mbar_arrive_expect_tx(
-                            full, static_cast<uint32_t>((nbox - nbad) * (D / 64) * box_rows * 128));
-                    }
-                    __syncwarp();
-                    // each lane issues the boxes of its page for every column block
-                    if (lane < nbox && !bad) {
-                        const int kk = key0 + lane * box_rows;
-                        const int row = (pg << ps_log2) + (kk & ps_mask);
+                __syncwarp();
+                if (lane < nbox && !bad) {
+                    const int kk = key0 + lane * box_rows;
+                    const int row = (pg_tile << ps_log2) + (kk & ps_mask);
 #pragma unroll
-                        for (int blk = 0; blk < D / 64; ++blk)
-                            tma_load_3d(dst + blk * Lo::BLK + lane * box_rows * 128,
-                                        kv ? &vmap : &kmap, full, blk * 64, g, row, pol_kv);
-                    }
-                } else {
-                    // small pages: gather 16-byte chunks, swizzle, zero rows past the sequence
-                    const __nv_bfloat16 *base = kv ? v_cache : k_cache;
-                    bool bad = false;
-                    for (int idx = lane; idx < BN * (D / 8); idx += 32) {
-                        const int key = idx / (D / 8), ch = idx % (D / 8);
-                        uint4 val = make_uint4(0u, 0u, 0u, 0u);
-                        if (key < nkeys) {
-                            const int kk = key0 + key;
-                            const int pg = prow[kk >> ps_log2];
-                            if (pg >= 0 && pg < num_pages) {
-                                const int64_t slot = ((int64_t)pg << ps_log2) + (kk & ps_mask);
-                                val = __ldg(reinterpret_cast<const uint4 *>(
-                                    base + (slot * Hkv + g) * D + ch * 8));
-                            } else {
-                                bad = true;
-                            }
-                        }
-                        *reinterpret_cast<uint4 *>(smem + (dst - smem_u32(smem)) +
-                                                   swz_offset(key, ch, BN)) = val;
-                    }
-                    if (__any_sync(0xffffffffu, bad) && lane == 0) *bad_page = 1;
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(full);
+                    for (int blk = 0; blk < D / 64; ++blk)
+                        tma_load_3d(dst + blk * Lo::KBLK + lane * box_rows * 128, kv ? &vmap : &kmap,
+                                    full, blk * 64, g, row, pol_kv);
                 }
+            } else {
+                // small pages: gather 16-byte chunks, swizzle, zero rows past the sequence
+                const __nv_bfloat16 *base = kv ? v_cache : k_cache;
+                bool bad = false;
+                for (int idx = lane; idx < BN * (D / 8); idx += 32) {
+                    const int key = idx / (D / 8), ch = idx % (D / 8);
+                    uint4 val = make_uint4(0u, 0u, 0u, 0u);
+                    if (key < nkeys) {
+                        const int kk = key0 + key;
+                        const int pg = prow[kk >> ps_log2];
+                        if (pg >= 0 && pg < num_pages) {
+                            const int64_t slot = ((int64_t)pg << ps_log2) + (kk & ps_mask);
+                            val = __ldg(reinterpret_cast<const uint4 *>(base + (slot * Hkv + g) * D +
+                                                                        ch * 8));
+                        } else {
+                            bad = true;
+                        }
+                    }
+                    *reinterpret_cast<uint4 *>(smem + (dst - smem_u32(smem)) +
+                                               swz_offset(key, ch, BN)) = val;
+                }
+                if (__any_sync(0xffffffffu, bad) && lane == 0) *bad_page = 1;
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(full);
             }
+            return true;
+        };
+        auto page_of_tile = [&](int j) -> int {
+            const int b0 = j * bpt;
+            if ((b0 >> 5) != w_cur) {
+                w_cur = b0 >> 5;
+                pg_cur = pg_nxt;
+                pg_nxt = load_window(w_cur + 1);
+            }
+            return __shfl_sync(0xffffffffu, pg_cur, (b0 + (lane % bpt)) & 31);
+        };
+        // K runs one tile ahead of V: K(j+1) is needed right after PV(j)
+        int pg_prev = page_of_tile(0);
+        bool ok = load_tile(0, 0, pg_prev);
+        for (int j = 0; ok && j < n_kt; ++j) {
+            const int pg_j = pg_prev;
+            if (j + 1 < n_kt) {
+                pg_prev = page_of_tile(j + 1);
+                ok = load_tile(0, j + 1, pg_prev);
+            }
+            ok = ok && load_tile(1, j, pg_j);
         }
-    } else if (warp == 1) {
+    } else if (warp == kMmaWarp) {
         // ================================================================ MMA issuer
         constexpr uint32_t idesc_s = instr_desc(BM, BN, false);
         constexpr uint32_t idesc_o = instr_desc(BM, D, true);
-        bool ok = mbar_wait_warp(BAR(B_QFULL), 0, abort_flag, dev_status);
-        auto issue_s = [&](int j) -> bool {
-            const int s = j % kStages, b = j & 1;
-            if (!mbar_wait_warp(BAR(B_KFULL(s)), (j / kStages) & 1, abort_flag, dev_status)) return false;
-            if (j >= 2 && !mbar_wait_warp(BAR(B_SFREE(b)), ((j - 2) >> 1) & 1, abort_flag, dev_status))
-                return false;
+        auto issue_s = [&](int qt, int j) {  // S(qt) = Q(qt) K(j)^T; K(j) is resident
+            const uint32_t kb = sK + (j % kKStages) * Lo::KV_BYTES;
+            const uint32_t qb = sQ + qt * Lo::Q_BYTES;
             tc_fence_after();
             if (lane == 0) {
-                const uint32_t kb = sK + s * Lo::KV_BYTES;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * Lo::BLK + (kk & 3) * 32;
-                    umma_bf16_ss(tm_s[b], smem_desc(sQ + off, 16, 1024), smem_desc(kb + off, 16, 1024),
-                                 idesc_s, kk > 0 ? 1u : 0u);
+                    const uint32_t qoff = (kk >> 2) * Lo::BLK + (kk & 3) * 32;
+                    const uint32_t koff = (kk >> 2) * Lo::KBLK + (kk & 3) * 32;
+                    umma_bf16_ss(tm_s(qt), smem_desc(qb + qoff, 16, 1024),
+                                 smem_desc(kb + koff, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
                 }
-                umma_commit(BAR(B_SFULL(b)));
-                umma_commit(BAR(B_KEMPTY(s)));
+                umma_commit(BAR(B_SFULL(qt)));
             }
             __syncwarp();
-            return true;
         };
-        if (ok) ok = issue_s(0);
+        auto issue_pv = [&](int qt, int j) {  // O(qt) += P(qt) V(j); P in TMEM, V in shared memory
+            const uint32_t vb = sV + (j % kVStages) * Lo::KV_BYTES;
+            tc_fence_after();
+            if (lane == 0) {
+#pragma unroll
+                for (int kk = 0; kk < BN / 16; ++kk)
+                    umma_bf16_ts(tm_o(qt), tm_s(qt) + kk * 8,
+                                 smem_desc(vb + kk * 16 * 128, Lo::KBLK, 1024), idesc_o,
+                                 (j > 0 || kk > 0) ? 1u : 0u);
+                umma_commit(BAR(B_ODONE(qt)));
+            }
+            __syncwarp();
+        };
+        bool ok = mbar_wait_warp(BAR(B_QFULL), 0, abort_flag, dev_status) &&
+                  mbar_wait_warp(BAR(B_KFULL(0)), 0, abort_flag, dev_status);
+        if (ok) {
+            for (int qt = 0; qt < NQ; ++qt)
+                if (nkt[qt] > 0) issue_s(qt, 0);
+            if (lane == 0) umma_commit(BAR(B_KEMPTY(0)));
+            __syncwarp();
+        }
         for (int j = 0; ok && j < n_kt; ++j) {
-            if (j + 1 < n_kt && !(ok = issue_s(j + 1))) break;
-            const int s = j % kStages;
-            if (!mbar_wait_warp(BAR(B_PFULL), j & 1, abort_flag, dev_status)) { ok = false; break; }
-            if (!mbar_wait_warp(BAR(B_VFULL(s)), (j / kStages) & 1, abort_flag, dev_status)) { ok = false; break; }
-            const uint32_t vb = sV + s * Lo::KV_BYTES;
+            const int s = j % kVStages;
+            const int s1 = (j + 1) % kKStages;
+            if (!mbar_wait_warp(BAR(B_VFULL(s)), (j / kVStages) & 1, abort_flag, dev_status)) {
+                ok = false;
+                break;
+            }
             if (j == n_kt - 1 && (j + 1) * BN > L) {
                 // keys past the sequence end hold stale pool data (maybe NaN):
                 // zero those V rows so that P = 0 there contributes exactly 0
+                const uint32_t vb = sV + s * Lo::KV_BYTES;
                 const int first = L - j * BN;
                 for (int idx = lane; idx < (BN - first) * (D / 8); idx += 32) {
                     const int key = first + idx / (D / 8), ch = idx % (D / 8);
@@ -326,142 +381,153 @@ __global__ void __launch_bounds__(kThreads, 1)
                 fence_proxy_async_smem();
                 __syncwarp();
             }
-            tc_fence_after();
-            if (lane == 0) {
+            const bool next = j + 1 < n_kt;
+            bool k_ready = false;
 #pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk) {
-                    const uint32_t aoff = (kk >> 2) * Lo::BLK + (kk & 3) * 32;  // P: K-major
-                    const uint32_t boff = kk * 16 * 128;                       // V: 16 keys per step
-                    umma_bf16_ss(tm_o, smem_desc(sP + aoff, 16, 1024),
-                                 smem_desc(vb + boff, Lo::BLK, 1024), idesc_o,
-                                 (j > 0 || kk > 0) ? 1u : 0u);
+            for (int qt = 0; qt < NQ; ++qt) {
+                if (j < nkt[qt]) {
+                    if (!mbar_wait_warp(BAR(B_PFULL(qt)), j & 1, abort_flag, dev_status)) {
+                        ok = false;
+                        break;
+                    }
+                    issue_pv(qt, j);
                 }
-                umma_commit(BAR(B_ODONE));
+                if (next && j + 1 < nkt[qt]) {
+                    if (!k_ready && !mbar_wait_warp(BAR(B_KFULL(s1)), ((j + 1) / kKStages) & 1,
+                                                    abort_flag, dev_status)) {
+                        ok = false;
+                        break;
+                    }
+                    k_ready = true;
+                    issue_s(qt, j + 1);
+                }
+            }
+            if (!ok) break;
+            if (lane == 0) {
                 umma_commit(BAR(B_VEMPTY(s)));
+                if (next) umma_commit(BAR(B_KEMPTY(s1)));
             }
             __syncwarp();
         }
-    } else if (warp >= 4) {
+    } else {
         // ================================================================ softmax
-        const int row = tid - 128;                 // TMEM lane == tile row
-        const int wq = warp - 4;                   // TMEM lane quarter of this warp
-        const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
-        const int tok = tok_begin + row / G;
-        const bool row_valid = tok < tok_end;
+        const int qt = warp >> 2;                  // query tile of this warpgroup
+        const int row = tid & 127;                 // TMEM lane == tile row
+        const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+        const int tok = tbeg[qt] + row / G;
+        const bool row_valid = tok < tend[qt];
         const int lim = c + tok;                   // last key this row may see
+        const int my_kt = nkt[qt];
         float m_ref = kNegBig, l_sum = 0.f;
         bool ok = true;
-        // tcgen05.ld/st are warp-collective: every wait outcome is made
-        // warp-uniform before the warp goes on to them.
-        for (int j = 0; j < n_kt; ++j) {
-            const int b = j & 1;
-            ok = mbar_wait_warp(BAR(B_SFULL(b)), (j >> 1) & 1, abort_flag, dev_status);
+        // tcgen05.ld/st are warp-collective: every wait outcome is warp-uniform
+        for (int j = 0; j < my_kt; ++j) {
+            // S(j) complete implies PV(j-1) complete: O is stable and P free
+            ok = mbar_wait_warp(BAR(B_SFULL(qt)), j & 1, abort_flag, dev_status);
             if (!ok) break;
             tc_fence_after();
+            // all 128 scores of this row in registers (one wait for four loads)
             uint32_t sv[BN];
 #pragma unroll
-            for (int cc = 0; cc < BN / 32; ++cc) tmem_ld_32cols(tm_s[b] + lane_off + cc * 32, sv + cc * 32);
+            for (int cc = 0; cc < BN / 32; ++cc) tmem_ld_32cols(tm_s(qt) + lane_off + cc * 32, sv + cc * 32);
             tmem_wait_ld();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(BAR(B_SFREE(b)));
-            // scores in the log2 domain, masked by selection
+            // causal mask by selection (-inf), only on tiles that cross some
+            // row's limit (a warp-uniform branch)
             const int key0 = j * BN;
-            float mt_max = kNegBig;
+            if (__any_sync(0xffffffffu, !row_valid || key0 + BN - 1 > lim)) {
+                const int nvalid = row_valid ? lim - key0 + 1 : 0;  // keys kept in this row
 #pragma unroll
-            for (int i = 0; i < BN; ++i) {
-                const bool v = row_valid && (key0 + i) <= lim;
-                const float x = v ? __uint_as_float(sv[i]) * scale_log2 : kNegBig;
-                sv[i] = __float_as_uint(x);
-                mt_max = fmaxf(mt_max, x);
+                for (int i = 0; i < BN; ++i)
+                    if (i >= nvalid) sv[i] = __float_as_uint(-INFINITY);
             }
+            float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+            for (int i = 0; i < BN; ++i) mx4[i & 3] = fmaxf(mx4[i & 3], __uint_as_float(sv[i]));
+            const float mt_max = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * scale_log2;
             const bool need = (j == 0) ? false : (mt_max > m_ref + kRescaleLog2);
             const bool warp_need = __any_sync(0xffffffffu, need);
             float alpha = 1.f;
             if (j == 0) {
-                m_ref = mt_max;
+                m_ref = fmaxf(mt_max, kNegBig);  // stays finite for rows with no key
             } else if (warp_need) {
                 const float mn = fmaxf(m_ref, mt_max);
                 alpha = ex2(m_ref - mn);
                 m_ref = mn;
             }
-            // probabilities, packed to bf16 pairs
-            uint32_t pk[BN / 2];
-            float rs = 0.f;
+            // p = 2^(s*scale*log2e - m_ref) on the SFU, packed to bf16 pairs and
+            // written 32 keys at a time into tensor memory over the S columns
+            // already read (keys 32cc.. -> columns 16cc..)
+            const float neg_m = -m_ref;
+            float rs4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int i = 0; i < BN; i += 2) {
-                const float x0 = __uint_as_float(sv[i]), x1 = __uint_as_float(sv[i + 1]);
-                const float p0 = (x0 > 0.5f * kNegBig) ? ex2(x0 - m_ref) : 0.f;
-                const float p1 = (x1 > 0.5f * kNegBig) ? ex2(x1 - m_ref) : 0.f;
-                rs += p0 + p1;
-                pk[i / 2] = pack_bf16x2(p0, p1);
+            for (int cc = 0; cc < BN / 32; ++cc) {
+                uint32_t pk[16];
+#pragma unroll
+                for (int q = 0; q < 16; ++q) {
+                    const int i = cc * 32 + 2 * q;
+                    const float p0 = ex2(fmaf(__uint_as_float(sv[i]), scale_log2, neg_m));
+                    const float p1 = ex2(fmaf(__uint_as_float(sv[i + 1]), scale_log2, neg_m));
+                    rs4[q & 3] += p0 + p1;
+                    pk[q] = pack_bf16x2(p0, p1);
+                }
+                tmem_st_16cols(tm_s(qt) + lane_off + cc * 16, pk);
             }
-            l_sum = l_sum * alpha + rs;
-            // previous PV must be done before P is overwritten and O rescaled
-            if (j > 0) {
-                ok = mbar_wait_warp(BAR(B_ODONE), (j - 1) & 1, abort_flag, dev_status);
-                if (!ok) break;
-                tc_fence_after();
-                if (warp_need) {
+            l_sum = l_sum * alpha + ((rs4[0] + rs4[1]) + (rs4[2] + rs4[3]));
+            // rescale the output row to the new reference (PV(j-1) is complete)
+            if (warp_need) {
 #pragma unroll
-                    for (int cc = 0; cc < D / 32; ++cc) {
-                        uint32_t ov[32];
-                        tmem_ld_32cols(tm_o + lane_off + cc * 32, ov);
-                        tmem_wait_ld();
+                for (int cc = 0; cc < D / 32; ++cc) {
+                    uint32_t ov[32];
+                    tmem_ld_32cols(tm_o(qt) + lane_off + cc * 32, ov);
+                    tmem_wait_ld();
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-                        tmem_st_32cols(tm_o + lane_off + cc * 32, ov);
-                    }
-                    tmem_wait_st();
+                    for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+                    tmem_st_32cols(tm_o(qt) + lane_off + cc * 32, ov);
                 }
             }
-            // P row -> shared memory, swizzled K-major (16 chunks of 8 keys)
-            uint8_t *pbase = smem + Lo::OFF_P;
-#pragma unroll
-            for (int ch = 0; ch < BN / 8; ++ch)
-                *reinterpret_cast<uint4 *>(pbase + swz_offset(row, ch, BM)) =
-                    make_uint4(pk[ch * 4 + 0], pk[ch * 4 + 1], pk[ch * 4 + 2], pk[ch * 4 + 3]);
-            fence_proxy_async_smem();
+            tmem_wait_st();  // P and O stores
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(BAR(B_PFULL));
+            if (lane == 0) mbar_arrive(BAR(B_PFULL(qt)));
         }
-        if (ok) ok = mbar_wait_warp(BAR(B_ODONE), (n_kt - 1) & 1, abort_flag, dev_status);
+        if (ok && my_kt > 0) ok = mbar_wait_warp(BAR(B_ODONE(qt)), (my_kt - 1) & 1, abort_flag, dev_status);
         tc_fence_after();
         __syncthreads();
         const bool poison = (*bad_page != 0) || (*abort_flag != 0) || !ok;
-        // every lane takes part in the warp-wide TMEM loads; only valid rows store
-        const float inv = row_valid ? 1.f / l_sum : 0.f;
-        __nv_bfloat16 *orow = out + ((int64_t)(cu0 + tok) * Hq + (int64_t)g * G + row % G) * D;
+        if (my_kt > 0) {
+            // every lane takes part in the warp-wide TMEM loads; only valid rows store
+            const float inv = row_valid ? 1.f / l_sum : 0.f;
+            __nv_bfloat16 *orow = out + ((int64_t)(cu0 + tok) * Hq + (int64_t)g * G + row % G) * D;
 #pragma unroll
-        for (int cc = 0; cc < D / 32; ++cc) {
-            uint32_t ov[32];
-            tmem_ld_32cols(tm_o + lane_off + cc * 32, ov);
-            tmem_wait_ld();
-            uint32_t pk[16];
+            for (int cc = 0; cc < D / 32; ++cc) {
+                uint32_t ov[32];
+                tmem_ld_32cols(tm_o(qt) + lane_off + cc * 32, ov);
+                tmem_wait_ld();
+                uint32_t pk[16];
 #pragma unroll
-            for (int e = 0; e < 32; e += 2) {
-                float a = __uint_as_float(ov[e]) * inv, bb = __uint_as_float(ov[e + 1]) * inv;
-                if (poison) a = bb = __int_as_float(0x7fc00000);
-                pk[e / 2] = pack_bf16x2(a, bb);
-            }
-            if (row_valid) {
+                for (int e = 0; e < 32; e += 2) {
+                    float a = __uint_as_float(ov[e]) * inv, bb = __uint_as_float(ov[e + 1]) * inv;
+                    if (poison) a = bb = __int_as_float(0x7fc00000);
+                    pk[e / 2] = pack_bf16x2(a, bb);
+                }
+                if (row_valid) {
 #pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4)
-                    reinterpret_cast<uint4 *>(orow + cc * 32)[q4] =
-                        make_uint4(pk[q4 * 4], pk[q4 * 4 + 1], pk[q4 * 4 + 2], pk[q4 * 4 + 3]);
+                    for (int q4 = 0; q4 < 4; ++q4)
+                        reinterpret_cast<uint4 *>(orow + cc * 32)[q4] =
+                            make_uint4(pk[q4 * 4], pk[q4 * 4 + 1], pk[q4 * 4 + 2], pk[q4 * 4 + 3]);
+                }
             }
         }
-        if (poison && tid == 128 && dev_status && *bad_page) atomicOr(dev_status, PKV_DEV_BAD_PAGE);
+        if (poison && tid == 0 && dev_status && *bad_page) atomicOr(dev_status, PKV_DEV_BAD_PAGE);
         tc_fence_before();
         __syncthreads();
         return;
     }
-    // producer, MMA and idle warps meet the softmax warps here, then free TMEM
+    // producer and MMA warps meet the softmax warps here, then free TMEM
     __syncthreads();
     tc_fence_before();
     __syncthreads();
-    if (warp == 1) {
+    if (warp == kMmaWarp) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
@@ -507,7 +573,7 @@ static pkv_status launch(const pkv_bf16 *q, const int32_t *cu, const pkv_bf16 *k
     }
     int ps_log2 = 0;
     while ((1 << ps_log2) < page_size) ++ps_log2;
-    const int mtiles = (max_q_len + TOK - 1) / TOK;
+    const int mtiles = (max_q_len + NQ * TOK - 1) / (NQ * TOK);
     const int64_t grid = static_cast<int64_t>(mtiles) * B * Hkv;
     if (grid == 0) return PKV_OK;
     if (grid > 0x7fffffffll) return PKV_EUNSUPPORTED;
