@@ -12,7 +12,7 @@
 // One block (one per SM) owns two 128-row query tiles, A and B, of one
 // request and one KV head; a tile holds 128/G consecutive new tokens x the G
 // query heads of that KV head, so every K/V tile staged in shared memory
-// serves 2 x 128 rows.  Roles (320 threads):
+// serves 2 x 128 rows.  Roles (352 threads):
 //   warp 8      producer: Q tiles A and B once, then 128-key K and V tiles
 //               through 2-stage rings, K one tile ahead of V.  Pages of >= 8 tokens come in as TMA
 //               boxes (one per page and 64-column block, 128-byte swizzle,
@@ -20,12 +20,12 @@
 //               pages are gathered by the warp's lanes with 16-byte loads and
 //               swizzled stores.  Page ids are read in warp-wide windows, one
 //               window ahead.
-//   warp 9      allocates all 512 TMEM columns (per query tile: a 128x128 fp32
-//               score buffer S, whose first 64 columns then hold P as bf16
-//               pairs, and a 128 x head_dim fp32 output accumulator O); one
-//               lane issues, in this order per key tile j,
-//                 O_A += P_A(j) V_j,  S_A(j+1) = Q_A K_(j+1)^T,
-//                 O_B += P_B(j) V_j,  S_B(j+1) = Q_B K_(j+1)^T,
+//   warps 9,10  warp 9 allocates all 512 TMEM columns (per query tile: a
+//               128x128 fp32 score buffer S, whose first 64 columns then hold
+//               P as bf16 pairs, and a 128 x head_dim fp32 output accumulator
+//               O); one lane of warp 9 + t issues the MMAs of tile t, in this
+//               order per key tile j:
+//                 O_t += P_t(j) V_j,  S_t(j+1) = Q_t K_(j+1)^T,
 //               with S from Q and K in shared memory (M=128, N=128,
 //               K=head_dim) and PV reading P from tensor memory and V from
 //               shared memory (M=128, N=head_dim, K=128).  Because the tensor
@@ -49,12 +49,12 @@
 namespace pkv {
 namespace prefill {
 
-constexpr int kThreads = 320;
+constexpr int kThreads = 352;
 constexpr int BM = 128;  // rows of a query tile: (token, head) pairs
 constexpr int NQ = 2;    // query tiles per block
 constexpr int BN = 128;  // keys per KV tile
 constexpr int kKStages = 2, kVStages = 2;
-constexpr int kProducerWarp = 8, kMmaWarp = 9;
+constexpr int kProducerWarp = 8, kMmaWarp = 9;  // warps 9 and 10 issue the MMAs of tiles A and B
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kNegBig = -1.0e30f;
 constexpr float kRescaleLog2 = 8.0f;  // lazy rescale threshold (factor 256)
@@ -183,11 +183,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(BAR(B_QFULL), 1);
         for (int s = 0; s < kKStages; ++s) {
             mbar_init(BAR(B_KFULL(s)), 1);
-            mbar_init(BAR(B_KEMPTY(s)), 1);
+            mbar_init(BAR(B_KEMPTY(s)), NQ);  // released by both MMA warps
         }
         for (int s = 0; s < kVStages; ++s) {
             mbar_init(BAR(B_VFULL(s)), 1);
-            mbar_init(BAR(B_VEMPTY(s)), 1);
+            mbar_init(BAR(B_VEMPTY(s)), NQ);
         }
         for (int qt = 0; qt < NQ; ++qt) {
             mbar_init(BAR(B_SFULL(qt)), 1);
@@ -320,11 +320,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             ok = ok && load_tile(1, j, pg_j);
         }
-    } else if (warp == kMmaWarp) {
-        // ================================================================ MMA issuer
+    } else if (warp >= kMmaWarp) {
+        // ================================================================ MMA issuers
+        // Warp 9 + qt issues the MMAs of query tile qt, so one tile's issue never
+        // waits behind the other's.  Both warps step through every key tile to
+        // release the K and V slots (count NQ) in phase.
+        const int qt = warp - kMmaWarp;
         constexpr uint32_t idesc_s = instr_desc(BM, BN, false);
         constexpr uint32_t idesc_o = instr_desc(BM, D, true);
-        auto issue_s = [&](int qt, int j) {  // S(qt) = Q(qt) K(j)^T; K(j) is resident
+        auto issue_s = [&](int j) {  // S(qt) = Q(qt) K(j)^T; K(j) is resident
             const uint32_t kb = sK + (j % kKStages) * Lo::KV_BYTES;
             const uint32_t qb = sQ + qt * Lo::Q_BYTES;
             tc_fence_after();
@@ -340,7 +344,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             __syncwarp();
         };
-        auto issue_pv = [&](int qt, int j) {  // O(qt) += P(qt) V(j); P in TMEM, V in shared memory
+        auto issue_pv = [&](int j) {  // O(qt) += P(qt) V(j); P in TMEM, V in shared memory
             const uint32_t vb = sV + (j % kVStages) * Lo::KV_BYTES;
             tc_fence_after();
             if (lane == 0) {
@@ -356,58 +360,50 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = mbar_wait_warp(BAR(B_QFULL), 0, abort_flag, dev_status) &&
                   mbar_wait_warp(BAR(B_KFULL(0)), 0, abort_flag, dev_status);
         if (ok) {
-            for (int qt = 0; qt < NQ; ++qt)
-                if (nkt[qt] > 0) issue_s(qt, 0);
+            if (nkt[qt] > 0) issue_s(0);
             if (lane == 0) umma_commit(BAR(B_KEMPTY(0)));
             __syncwarp();
         }
         for (int j = 0; ok && j < n_kt; ++j) {
             const int s = j % kVStages;
-            const int s1 = (j + 1) % kKStages;
             if (!mbar_wait_warp(BAR(B_VFULL(s)), (j / kVStages) & 1, abort_flag, dev_status)) {
                 ok = false;
                 break;
             }
-            if (j == n_kt - 1 && (j + 1) * BN > L) {
-                // keys past the sequence end hold stale pool data (maybe NaN):
-                // zero those V rows so that P = 0 there contributes exactly 0
-                const uint32_t vb = sV + s * Lo::KV_BYTES;
-                const int first = L - j * BN;
-                for (int idx = lane; idx < (BN - first) * (D / 8); idx += 32) {
-                    const int key = first + idx / (D / 8), ch = idx % (D / 8);
-                    *reinterpret_cast<uint4 *>(smem + (vb - smem_u32(smem)) + swz_offset(key, ch, BN)) =
-                        make_uint4(0u, 0u, 0u, 0u);
+            if (j < nkt[qt]) {
+                if (j == n_kt - 1 && (j + 1) * BN > L) {
+                    // keys past the sequence end hold stale pool data (maybe NaN):
+                    // zero those V rows so that P = 0 there contributes exactly 0
+                    // (both MMA warps write the same zeros before their own PV)
+                    const uint32_t vb = sV + s * Lo::KV_BYTES;
+                    const int first = L - j * BN;
+                    for (int idx = lane; idx < (BN - first) * (D / 8); idx += 32) {
+                        const int key = first + idx / (D / 8), ch = idx % (D / 8);
+                        *reinterpret_cast<uint4 *>(smem + (vb - smem_u32(smem)) +
+                                                   swz_offset(key, ch, BN)) = make_uint4(0u, 0u, 0u, 0u);
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
                 }
-                fence_proxy_async_smem();
+                if (!mbar_wait_warp(BAR(B_PFULL(qt)), j & 1, abort_flag, dev_status)) {
+                    ok = false;
+                    break;
+                }
+                issue_pv(j);
+            }
+            if (lane == 0) umma_commit(BAR(B_VEMPTY(s)));
+            __syncwarp();
+            if (j + 1 < n_kt) {
+                const int s1 = (j + 1) % kKStages;
+                if (!mbar_wait_warp(BAR(B_KFULL(s1)), ((j + 1) / kKStages) & 1, abort_flag,
+                                    dev_status)) {
+                    ok = false;
+                    break;
+                }
+                if (j + 1 < nkt[qt]) issue_s(j + 1);
+                if (lane == 0) umma_commit(BAR(B_KEMPTY(s1)));
                 __syncwarp();
             }
-            const bool next = j + 1 < n_kt;
-            bool k_ready = false;
-#pragma unroll
-            for (int qt = 0; qt < NQ; ++qt) {
-                if (j < nkt[qt]) {
-                    if (!mbar_wait_warp(BAR(B_PFULL(qt)), j & 1, abort_flag, dev_status)) {
-                        ok = false;
-                        break;
-                    }
-                    issue_pv(qt, j);
-                }
-                if (next && j + 1 < nkt[qt]) {
-                    if (!k_ready && !mbar_wait_warp(BAR(B_KFULL(s1)), ((j + 1) / kKStages) & 1,
-                                                    abort_flag, dev_status)) {
-                        ok = false;
-                        break;
-                    }
-                    k_ready = true;
-                    issue_s(qt, j + 1);
-                }
-            }
-            if (!ok) break;
-            if (lane == 0) {
-                umma_commit(BAR(B_VEMPTY(s)));
-                if (next) umma_commit(BAR(B_KEMPTY(s1)));
-            }
-            __syncwarp();
         }
     } else {
         // ================================================================ softmax
@@ -442,7 +438,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-            for (int i = 0; i < BN; ++i) mx4[i & 3] = fmaxf(mx4[i & 3], __uint_as_float(sv[i]));
+            for (int i = 0; i < BN; i += 2)
+                mx4[(i >> 1) & 3] = fmax3(mx4[(i >> 1) & 3], __uint_as_float(sv[i]), __uint_as_float(sv[i + 1]));
             const float mt_max = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * scale_log2;
             const bool need = (j == 0) ? false : (mt_max > m_ref + kRescaleLog2);
             const bool warp_need = __any_sync(0xffffffffu, need);
@@ -458,21 +455,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             // written 32 keys at a time into tensor memory over the S columns
             // already read (keys 32cc.. -> columns 16cc..)
             const float neg_m = -m_ref;
-            float rs4[4] = {0.f, 0.f, 0.f, 0.f};
+            float rs[4] = {0.f, 0.f, 0.f, 0.f};  // two packed pairs of partial sums
 #pragma unroll
             for (int cc = 0; cc < BN / 32; ++cc) {
                 uint32_t pk[16];
 #pragma unroll
                 for (int q = 0; q < 16; ++q) {
                     const int i = cc * 32 + 2 * q;
-                    const float p0 = ex2(fmaf(__uint_as_float(sv[i]), scale_log2, neg_m));
-                    const float p1 = ex2(fmaf(__uint_as_float(sv[i + 1]), scale_log2, neg_m));
-                    rs4[q & 3] += p0 + p1;
+                    float x0, x1;
+                    fma2(x0, x1, __uint_as_float(sv[i]), __uint_as_float(sv[i + 1]), scale_log2,
+                         scale_log2, neg_m, neg_m);
+                    const float p0 = ex2(x0), p1 = ex2(x1);
+                    add2(rs[2 * (q & 1)], rs[2 * (q & 1) + 1], p0, p1);
                     pk[q] = pack_bf16x2(p0, p1);
                 }
                 tmem_st_16cols(tm_s(qt) + lane_off + cc * 16, pk);
             }
-            l_sum = l_sum * alpha + ((rs4[0] + rs4[1]) + (rs4[2] + rs4[3]));
+            l_sum = l_sum * alpha + ((rs[0] + rs[1]) + (rs[2] + rs[3]));
             // rescale the output row to the new reference (PV(j-1) is complete)
             if (warp_need) {
 #pragma unroll
