@@ -16,6 +16,11 @@ then paged decode attention (main kernel + log-sum-exp merge).
   prefill   the ragged-prefill workload (8 requests, 128..2048 new tokens,
             0-50 % cached prefix) in TFLOP/s against the measured bf16 peak,
             L2 flushed between repetitions
+  long_decode   the Llama-3.2-1B-shaped long-context decode (8 sequences of
+                16K-32K keys, page_size 256): decode call GB/s, L2 flushed
+  mixed_step    the continuous-batching step over 28 layers (kv_store of 1280
+                new tokens, 4-chunk prefill, 256-sequence decode per layer, each
+                layer its own KV pool), eager and CUDA-graph replayed
   cpu_baseline  the CPU oracle on a bounded sample of the same step
 
 --impl reference times the CPU oracle on the same workload (bounded samples).
@@ -272,8 +277,13 @@ def run_gpu(args, rank, world):
     e2e_ms = reduce_max(e0.elapsed_time(e1) / args.steps, world)
     assert int(status.item()) == 0
 
-    # ---- prefill TFLOP/s on the ragged-prefill workload (rank 0 reports)
-    prefill = time_prefill(args, dev, stream, bf16_peak, bf16_sus, peak_kind) if rank == 0 else None
+    # ---- prefill TFLOP/s on the ragged-prefill workload, the long-context decode
+    # and the mixed continuous-batching step (rank 0 reports)
+    prefill = long_dec = mixed = None
+    if rank == 0:
+        prefill = time_prefill(args, dev, stream, bf16_peak, bf16_sus, peak_kind)
+        long_dec = time_long_decode(args, dev, stream, hbm_peak, peak_kind)
+        mixed = time_mixed_step(args, dev, stream)
 
     value = world * B_step / (ms_all * 1e-3) / 1e9
     dec_gbs = B_dec / (dec_ms * 1e-3) / 1e9
@@ -327,6 +337,8 @@ def run_gpu(args, rank, world):
     }
     if prefill is not None:
         line["prefill"] = prefill
+        line["long_decode"] = long_dec
+        line["mixed_step"] = mixed
     return line
 
 
@@ -366,6 +378,116 @@ def time_prefill(args, dev, stream, bf16_peak, bf16_sus, peak_kind):
             "tflops": round(tf, 2), "ms": round(ms, 5), "flops": fl,
             "peak": bf16_peak, "peak_kind": f"{peak_kind} bf16 dense burst",
             "frac": round(tf / bf16_peak, 4), "l2": "flushed (512 MB write) before each rep"}
+
+
+def time_long_decode(args, dev, stream, hbm_peak, peak_kind):
+    """Decode call alone on the Llama-3.2-1B-shaped long-context workload."""
+    import torch
+    import paged_kv_cache_out_gb300 as pkv
+    from synth import make_config
+
+    x = make_config("llama_long_decode", seed=args.seed)
+    k, v = to_dev(x.k_cache, dev), to_dev(x.v_cache, dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    pkv.kv_store(to_dev(x.k_new, dev), to_dev(x.v_new, dev), to_dev(x.out_loc, dev), k, v,
+                 dev_status=status, stream=stream)
+    q, pt, sl = to_dev(x.q, dev), to_dev(x.page_table, dev), to_dev(x.seq_lens, dev)
+    out = torch.empty_like(q)
+    ws = pkv.decode_workspace(x.B, x.Hq, x.Hkv, x.d, dev)
+    reps = max(20, min(args.steps, 500))
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    times = []
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup + reps):
+            flush.zero_()  # the pool (0.4 GB) is larger than L2, the flush keeps reps cold
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            pkv.paged_decode_attn(q, k, v, pt, sl, x.scale, workspace=ws, dev_status=status,
+                                  out=out, stream=stream)
+            b.record(stream)
+            if i >= args.warmup:
+                times.append((a, b))
+        stream.synchronize()
+    assert int(status.item()) == 0
+    ms = statistics.median(a.elapsed_time(b) for a, b in times)
+    nb = decode_bytes(x)
+    gbs = nb / (ms * 1e-3) / 1e9
+    return {"workload": f"llama_long_decode: B={x.B}, Hq={x.Hq}, Hkv={x.Hkv}, d={x.d}, "
+                        f"page_size={x.page_size}, kv tokens={int(x.seq_lens.sum())}",
+            "gbs": round(gbs, 2), "ms": round(ms, 5), "bytes": nb, "peak": hbm_peak,
+            "peak_kind": f"{peak_kind} HBM copy GB/s", "frac": round(gbs / hbm_peak, 4),
+            "tokens_per_s": round(x.B / (ms * 1e-3), 1),
+            "l2": "flushed (512 MB write) before each rep"}
+
+
+def time_mixed_step(args, dev, stream):
+    """The continuous-batching step: per layer kv_store of all new tokens, prefill
+    of the chunks, decode of the rest; 28 layers, each with its own KV pool."""
+    import torch
+    import paged_kv_cache_out_gb300 as pkv
+    from synth import make_config
+
+    x = make_config("mixed_step", seed=args.seed)
+    layers = x.meta["layers"]
+    npre = x.meta["n_prefill"]
+    t_pre = int(x.cu_seqlens_q[npre])
+    k0, v0 = to_dev(x.k_cache, dev), to_dev(x.v_cache, dev)
+    pools = [(k0.clone(), v0.clone()) for _ in range(layers)]
+    del k0, v0
+    q, kn, vn = to_dev(x.q, dev), to_dev(x.k_new, dev), to_dev(x.v_new, dev)
+    loc, pt, sl, cu = (to_dev(x.out_loc, dev), to_dev(x.page_table, dev), to_dev(x.seq_lens, dev),
+                       to_dev(x.cu_seqlens_q, dev))
+    pre_max_q = int(x.new_lens[:npre].max())
+    out = torch.empty_like(q)
+    ws = pkv.decode_workspace(x.B - npre, x.Hq, x.Hkv, x.d, dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def step():
+        for k, v in pools:
+            pkv.kv_store(kn, vn, loc, k, v, dev_status=status, stream=stream)
+            pkv.paged_prefill_attn(q[:t_pre], cu[:npre + 1], k, v, pt[:npre], sl[:npre], x.scale,
+                                   pre_max_q, dev_status=status, out=out[:t_pre], stream=stream)
+            pkv.paged_decode_attn(q[t_pre:], k, v, pt[npre:], sl[npre:], x.scale, workspace=ws,
+                                  dev_status=status, out=out[t_pre:], stream=stream)
+
+    reps = max(5, min(args.steps, 50))
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+        stream.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            step()
+        e1.record(stream)
+        stream.synchronize()
+    eager_ms = e0.elapsed_time(e1) / reps
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        step()
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            g.replay()
+        stream.synchronize()
+        e0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        e1.record(stream)
+        stream.synchronize()
+    graph_ms = e0.elapsed_time(e1) / reps
+    assert int(status.item()) == 0
+    dec = x.subset(npre, x.B)
+    nbytes = layers * (decode_bytes(dec) + store_bytes(x))
+    fl = layers * prefill_flops(x.subset(0, npre))
+    del pools
+    torch.cuda.empty_cache()
+    return {"workload": f"mixed_step x{layers} layers: {npre} prefill chunks ({t_pre} tokens) + "
+                        f"{x.B - npre} decode seqs (kv tokens {int(dec.seq_lens.sum())}), Qwen3 heads, "
+                        f"page_size 16, one KV pool per layer",
+            "ms_per_step_eager": round(eager_ms, 4), "ms_per_step_graph": round(graph_ms, 4),
+            "tokens_per_s": round(x.Tq / (graph_ms * 1e-3), 1),
+            "decode_plus_store_gbs": round(nbytes / (graph_ms * 1e-3) / 1e9, 1),
+            "prefill_flops_per_step": fl, "launches_per_step": 5 * layers}
 
 
 def reduce_max(v, world):
