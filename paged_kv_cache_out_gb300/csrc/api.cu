@@ -68,10 +68,15 @@ bool encode_kv_map(CUtensorMap *map, const void *base, int64_t num_slots, int nu
     cuuint64_t strides[2] = {(cuuint64_t)head_dim * 2, (cuuint64_t)head_dim * num_kv_heads * 2};
     cuuint32_t box[3] = {(cuuint32_t)box_inner, 1u, (cuuint32_t)box_rows};
     cuuint32_t estr[3] = {1u, 1u, 1u};
+    // L2 promotion no wider than one head's row: the rows of one head are
+    // num_kv_heads * head_dim * 2 bytes apart, so a wider promotion would
+    // fetch the neighbouring head's row, which this copy does not use
+    const CUtensorMapL2promotion promo = head_dim * 2 >= 256 ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B
+                                                             : CU_TENSOR_MAP_L2_PROMOTION_L2_128B;
     CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims,
                      strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                     swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
-                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                     swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE, promo,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 

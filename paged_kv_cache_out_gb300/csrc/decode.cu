@@ -308,8 +308,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int grp = warp * S::ROWS_PER_WARP + lane / R;  // row-group of this lane
     const int lr = lane % R;                             // 16-byte slice within a row
     const int ctid = tid;                                // 0..127
-    float qf[G][8];
-    float m[G], l[G], o[G][8];
+    // q (pre-scaled by scale*log2 e) and the output slice as fp32 pairs, so the
+    // dot products and the value accumulation run as packed fp32x2 FMAs
+    float2 q2[G][4];
+    float m[G], l[G];
+    float2 o2[G][4];
     int64_t pos = my_start;
     Piece p;
     uint32_t it = 0;
@@ -321,7 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             m[h] = kNegBig;
             l[h] = 0.f;
 #pragma unroll
-            for (int e = 0; e < 8; ++e) o[h][e] = 0.f;
+            for (int e = 0; e < 4; ++e) o2[h][e] = make_float2(0.f, 0.f);
         }
         bool bad_piece = false;
         for (int tile = p.t0; tile < p.t1; ++tile, ++it) {
@@ -337,36 +340,32 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (flags[s]) bad_piece = true;
             if (tile == p.t0) {
                 const uint32_t qbase = kbase + 2 * S::TILE_BYTES;
+                const float2 sc2 = make_float2(scale_log2, scale_log2);
 #pragma unroll
                 for (int h = 0; h < G; ++h) {
                     const uint4 w = lds128(qbase + (h * D + lr * 8) * 2);
-                    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        qf[h][2 * e] = bf16lo(ws[e]) * scale_log2;
-                        qf[h][2 * e + 1] = bf16hi(ws[e]) * scale_log2;
-                    }
+                    q2[h][0] = fmul2(bf16x2_to_f2(w.x), sc2);
+                    q2[h][1] = fmul2(bf16x2_to_f2(w.y), sc2);
+                    q2[h][2] = fmul2(bf16x2_to_f2(w.z), sc2);
+                    q2[h][3] = fmul2(bf16x2_to_f2(w.w), sc2);
                 }
             }
             const int tok0 = tile * T;
+            const bool full_tile = tok0 + T <= L;  // same for the whole block: no row masking
             float sc[U][G];
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const int row = grp + u * GROUPS;
                 const uint4 w = lds128(kbase + (row * D + lr * 8) * 2);
-                const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-                float kf[8];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    kf[2 * e] = bf16lo(ws[e]);
-                    kf[2 * e + 1] = bf16hi(ws[e]);
-                }
+                const float2 k0 = bf16x2_to_f2(w.x), k1 = bf16x2_to_f2(w.y);
+                const float2 k2 = bf16x2_to_f2(w.z), k3 = bf16x2_to_f2(w.w);
 #pragma unroll
                 for (int h = 0; h < G; ++h) {
-                    float acc = 0.f;
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) acc = fmaf(qf[h][e], kf[e], acc);
-                    sc[u][h] = acc;
+                    float2 acc = fmul2(q2[h][0], k0);
+                    acc = ffma2(q2[h][1], k1, acc);
+                    acc = ffma2(q2[h][2], k2, acc);
+                    acc = ffma2(q2[h][3], k3, acc);
+                    sc[u][h] = acc.x + acc.y;
                 }
             }
 #pragma unroll
@@ -377,45 +376,56 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int h = 0; h < G; ++h)
                         sc[u][h] += __shfl_xor_sync(0xffffffffu, sc[u][h], off);
             }
-            bool valid[U];
+            if (!full_tile) {
+                // rows past the sequence end: score -inf, so p = 0
 #pragma unroll
-            for (int u = 0; u < U; ++u) valid[u] = (tok0 + grp + u * GROUPS) < L;
+                for (int u = 0; u < U; ++u)
+                    if (tok0 + grp + u * GROUPS >= L)
+#pragma unroll
+                        for (int h = 0; h < G; ++h) sc[u][h] = -INFINITY;
+            }
+            // online softmax with a lazy reference: the running max m only moves
+            // when a score exceeds it by more than 2^8, so p <= 256 and the
+            // rescaling of l and o is rare (exact: every term shares m)
             float pr[U][G];
 #pragma unroll
             for (int h = 0; h < G; ++h) {
-                float mt = kNegBig;
+                float mt = sc[0][h];
 #pragma unroll
-                for (int u = 0; u < U; ++u)
-                    if (valid[u]) mt = fmaxf(mt, sc[u][h]);
-                const float mn = fmaxf(m[h], mt);
-                const float alpha = ex2(m[h] - mn);
-                m[h] = mn;
+                for (int u = 1; u < U; ++u) mt = fmaxf(mt, sc[u][h]);
+                if (mt > m[h] + 8.0f) {
+                    const float alpha = ex2(m[h] - mt);
+                    m[h] = mt;
+                    l[h] *= alpha;
+                    const float2 a2 = make_float2(alpha, alpha);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) o2[h][e] = fmul2(o2[h][e], a2);
+                }
                 float sum = 0.f;
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
-                    pr[u][h] = valid[u] ? ex2(sc[u][h] - mn) : 0.f;
+                    pr[u][h] = ex2(sc[u][h] - m[h]);
                     sum += pr[u][h];
                 }
-                l[h] = l[h] * alpha + sum;
-#pragma unroll
-                for (int e = 0; e < 8; ++e) o[h][e] *= alpha;
+                l[h] += sum;
             }
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const int row = grp + u * GROUPS;
-                const uint4 w = lds128(vbase + (row * D + lr * 8) * 2);
-                const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-                float vf[8];
+                uint4 w = lds128(vbase + (row * D + lr * 8) * 2);
+                // rows past the sequence end hold stale data (maybe NaN): zero
+                // them, since 0 * NaN would poison the sum
+                if (!full_tile && tok0 + row >= L) w = make_uint4(0u, 0u, 0u, 0u);
+                const float2 v0 = bf16x2_to_f2(w.x), v1 = bf16x2_to_f2(w.y);
+                const float2 v2 = bf16x2_to_f2(w.z), v3 = bf16x2_to_f2(w.w);
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    // rows past the sequence end hold stale data: select, never multiply
-                    vf[2 * e] = valid[u] ? bf16lo(ws[e]) : 0.f;
-                    vf[2 * e + 1] = valid[u] ? bf16hi(ws[e]) : 0.f;
+                for (int h = 0; h < G; ++h) {
+                    const float2 p2 = make_float2(pr[u][h], pr[u][h]);
+                    o2[h][0] = ffma2(p2, v0, o2[h][0]);
+                    o2[h][1] = ffma2(p2, v1, o2[h][1]);
+                    o2[h][2] = ffma2(p2, v2, o2[h][2]);
+                    o2[h][3] = ffma2(p2, v3, o2[h][3]);
                 }
-#pragma unroll
-                for (int h = 0; h < G; ++h)
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) o[h][e] = fmaf(pr[u][h], vf[e], o[h][e]);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&bars[STAGES + s]));
@@ -426,7 +436,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int h = 0; h < G; ++h) {
 #pragma unroll
-            for (int e = 0; e < 8; ++e) red_o[(grp * G + h) * D + lr * 8 + e] = o[h][e];
+            for (int e = 0; e < 4; ++e) {
+                red_o[(grp * G + h) * D + lr * 8 + 2 * e] = o2[h][e].x;
+                red_o[(grp * G + h) * D + lr * 8 + 2 * e + 1] = o2[h][e].y;
+            }
             if (lr == 0) {
                 red_ml[(grp * G + h) * 2 + 0] = m[h];
                 red_ml[(grp * G + h) * 2 + 1] = l[h];
