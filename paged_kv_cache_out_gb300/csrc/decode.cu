@@ -40,10 +40,16 @@ constexpr int kCtasPerSm = 2;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kNegBig = -1.0e30f;  // running-max start: finite, so 2^(m - m') never is NaN
 
-template <int D>
+// A consumer lane owns EPL elements of a row (EPL/8 16-byte chunks): 16 when
+// there are at most 2 query heads per KV head (fewer lanes per row, so fewer
+// shuffle levels to reduce the dot products), else 8, which keeps 4 heads
+// within the registers of two blocks per SM.
+template <int D, int G>
 struct Shape {
     static constexpr int T = (D == 128) ? 32 : 64;  // key tokens per tile
-    static constexpr int R = D / 8;                  // lanes per K/V row (16 B each)
+    static constexpr int EPL = (G <= 2) ? 16 : 8;    // elements per lane
+    static constexpr int NCH = EPL / 8;               // 16-byte chunks per lane
+    static constexpr int R = D / EPL;                 // lanes per K/V row
     static constexpr int ROWS_PER_WARP = 32 / R;
     static constexpr int GROUPS = kConsumerWarps * ROWS_PER_WARP;
     static constexpr int U = T / GROUPS;  // rows of a tile per row-group
@@ -53,7 +59,7 @@ struct Shape {
 
 template <int D, int G>
 struct Smem {
-    using S = Shape<D>;
+    using S = Shape<D, G>;
     static constexpr int Q_BYTES = ((G * D * 2 + 127) / 128) * 128;
     static constexpr int STAGE_BYTES = 2 * S::TILE_BYTES + Q_BYTES;
     static constexpr int RING = S::STAGES * STAGE_BYTES;
@@ -162,16 +168,17 @@ __device__ void build_prefix(int32_t *prefix, int32_t *lens, const int32_t *seq_
 }
 
 template <int D, int G>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, G <= 4 ? kCtasPerSm : 1)
     decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                   const __nv_bfloat16 *__restrict__ q, const int32_t *__restrict__ page_table,
                   int64_t pt_stride, const int32_t *__restrict__ seq_lens, int B, int Hkv,
                   int ps_log2, int box_rows, int64_t num_pages, float scale_log2,
                   float *__restrict__ ws_part, int32_t *__restrict__ ws_prefix,
                   int32_t *dev_status, __nv_bfloat16 *__restrict__ out) {
-    using S = Shape<D>;
+    using S = Shape<D, G>;
     using M = Smem<D, G>;
     constexpr int T = S::T, R = S::R, U = S::U, GROUPS = S::GROUPS, STAGES = S::STAGES;
+    constexpr int NCH = S::NCH;
     const int Hq = Hkv * G;
     const int64_t cap = pt_stride << ps_log2;
 
@@ -306,13 +313,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // ---------------------------------------------------------------- consumers
     const int grp = warp * S::ROWS_PER_WARP + lane / R;  // row-group of this lane
-    const int lr = lane % R;                             // 16-byte slice within a row
+    const int lr = lane % R;                             // slice of a row
+    // the lane owns 16-byte chunks lr, lr + R, ... of each row
     const int ctid = tid;                                // 0..127
     // q (pre-scaled by scale*log2 e) and the output slice as fp32 pairs, so the
     // dot products and the value accumulation run as packed fp32x2 FMAs
-    float2 q2[G][4];
+    float2 q2[G][4 * NCH];
     float m[G], l[G];
-    float2 o2[G][4];
+    float2 o2[G][4 * NCH];
     int64_t pos = my_start;
     Piece p;
     uint32_t it = 0;
@@ -324,7 +332,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             m[h] = kNegBig;
             l[h] = 0.f;
 #pragma unroll
-            for (int e = 0; e < 4; ++e) o2[h][e] = make_float2(0.f, 0.f);
+            for (int e = 0; e < 4 * NCH; ++e) o2[h][e] = make_float2(0.f, 0.f);
         }
         bool bad_piece = false;
         for (int tile = p.t0; tile < p.t1; ++tile, ++it) {
@@ -342,13 +350,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t qbase = kbase + 2 * S::TILE_BYTES;
                 const float2 sc2 = make_float2(scale_log2, scale_log2);
 #pragma unroll
-                for (int h = 0; h < G; ++h) {
-                    const uint4 w = lds128(qbase + (h * D + lr * 8) * 2);
-                    q2[h][0] = fmul2(bf16x2_to_f2(w.x), sc2);
-                    q2[h][1] = fmul2(bf16x2_to_f2(w.y), sc2);
-                    q2[h][2] = fmul2(bf16x2_to_f2(w.z), sc2);
-                    q2[h][3] = fmul2(bf16x2_to_f2(w.w), sc2);
-                }
+                for (int h = 0; h < G; ++h)
+#pragma unroll
+                    for (int k = 0; k < NCH; ++k) {
+                        const uint4 w = lds128(qbase + (h * D + (lr + k * R) * 8) * 2);
+                        q2[h][4 * k + 0] = fmul2(bf16x2_to_f2(w.x), sc2);
+                        q2[h][4 * k + 1] = fmul2(bf16x2_to_f2(w.y), sc2);
+                        q2[h][4 * k + 2] = fmul2(bf16x2_to_f2(w.z), sc2);
+                        q2[h][4 * k + 3] = fmul2(bf16x2_to_f2(w.w), sc2);
+                    }
             }
             const int tok0 = tile * T;
             const bool full_tile = tok0 + T <= L;  // same for the whole block: no row masking
@@ -356,15 +366,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const int row = grp + u * GROUPS;
-                const uint4 w = lds128(kbase + (row * D + lr * 8) * 2);
-                const float2 k0 = bf16x2_to_f2(w.x), k1 = bf16x2_to_f2(w.y);
-                const float2 k2 = bf16x2_to_f2(w.z), k3 = bf16x2_to_f2(w.w);
+                float2 kv[4 * NCH];
+#pragma unroll
+                for (int k = 0; k < NCH; ++k) {
+                    const uint4 w = lds128(kbase + (row * D + (lr + k * R) * 8) * 2);
+                    kv[4 * k + 0] = bf16x2_to_f2(w.x);
+                    kv[4 * k + 1] = bf16x2_to_f2(w.y);
+                    kv[4 * k + 2] = bf16x2_to_f2(w.z);
+                    kv[4 * k + 3] = bf16x2_to_f2(w.w);
+                }
 #pragma unroll
                 for (int h = 0; h < G; ++h) {
-                    float2 acc = fmul2(q2[h][0], k0);
-                    acc = ffma2(q2[h][1], k1, acc);
-                    acc = ffma2(q2[h][2], k2, acc);
-                    acc = ffma2(q2[h][3], k3, acc);
+                    float2 acc = fmul2(q2[h][0], kv[0]);
+#pragma unroll
+                    for (int e = 1; e < 4 * NCH; ++e) acc = ffma2(q2[h][e], kv[e], acc);
                     sc[u][h] = acc.x + acc.y;
                 }
             }
@@ -399,7 +414,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     l[h] *= alpha;
                     const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) o2[h][e] = fmul2(o2[h][e], a2);
+                    for (int e = 0; e < 4 * NCH; ++e) o2[h][e] = fmul2(o2[h][e], a2);
                 }
                 float sum = 0.f;
 #pragma unroll
@@ -412,19 +427,24 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const int row = grp + u * GROUPS;
-                uint4 w = lds128(vbase + (row * D + lr * 8) * 2);
                 // rows past the sequence end hold stale data (maybe NaN): zero
                 // them, since 0 * NaN would poison the sum
-                if (!full_tile && tok0 + row >= L) w = make_uint4(0u, 0u, 0u, 0u);
-                const float2 v0 = bf16x2_to_f2(w.x), v1 = bf16x2_to_f2(w.y);
-                const float2 v2 = bf16x2_to_f2(w.z), v3 = bf16x2_to_f2(w.w);
+                const bool dead = !full_tile && tok0 + row >= L;
+                float2 vv[4 * NCH];
+#pragma unroll
+                for (int k = 0; k < NCH; ++k) {
+                    uint4 w = lds128(vbase + (row * D + (lr + k * R) * 8) * 2);
+                    if (dead) w = make_uint4(0u, 0u, 0u, 0u);
+                    vv[4 * k + 0] = bf16x2_to_f2(w.x);
+                    vv[4 * k + 1] = bf16x2_to_f2(w.y);
+                    vv[4 * k + 2] = bf16x2_to_f2(w.z);
+                    vv[4 * k + 3] = bf16x2_to_f2(w.w);
+                }
 #pragma unroll
                 for (int h = 0; h < G; ++h) {
                     const float2 p2 = make_float2(pr[u][h], pr[u][h]);
-                    o2[h][0] = ffma2(p2, v0, o2[h][0]);
-                    o2[h][1] = ffma2(p2, v1, o2[h][1]);
-                    o2[h][2] = ffma2(p2, v2, o2[h][2]);
-                    o2[h][3] = ffma2(p2, v3, o2[h][3]);
+#pragma unroll
+                    for (int e = 0; e < 4 * NCH; ++e) o2[h][e] = ffma2(p2, vv[e], o2[h][e]);
                 }
             }
             __syncwarp();
@@ -436,10 +456,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int h = 0; h < G; ++h) {
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                red_o[(grp * G + h) * D + lr * 8 + 2 * e] = o2[h][e].x;
-                red_o[(grp * G + h) * D + lr * 8 + 2 * e + 1] = o2[h][e].y;
-            }
+            for (int k = 0; k < NCH; ++k)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    red_o[(grp * G + h) * D + (lr + k * R) * 8 + 2 * e] = o2[h][4 * k + e].x;
+                    red_o[(grp * G + h) * D + (lr + k * R) * 8 + 2 * e + 1] = o2[h][4 * k + e].y;
+                }
             if (lr == 0) {
                 red_ml[(grp * G + h) * 2 + 0] = m[h];
                 red_ml[(grp * G + h) * 2 + 1] = l[h];
@@ -483,7 +505,7 @@ __global__ void __launch_bounds__(128)
     decode_merge_kernel(const int32_t *__restrict__ seq_lens, const int32_t *__restrict__ ws_prefix,
                         const float *__restrict__ ws_part, int B, int Hkv, int64_t cap, int grid,
                         int32_t *dev_status, __nv_bfloat16 *__restrict__ out) {
-    using S = Shape<D>;
+    using S = Shape<D, G>;
     grid_dependency_wait();  // partial states come from the main kernel
     const int b = blockIdx.x / Hkv, g = blockIdx.x % Hkv;
     const int Hq = Hkv * G;
@@ -569,7 +591,7 @@ static pkv_status launch(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_b
     if (!pkv_host::current_device(&dev)) return PKV_ECUDA;
     int ctas = 0;
     if (!prepare<D, G>(dev, B, &ctas)) return PKV_ECUDA;
-    const int T = Shape<D>::T;
+    const int T = Shape<D, G>::T;
     const int box_rows = page_size < T ? page_size : T;
     CUtensorMap kmap, vmap;
     const int64_t slots = num_pages * page_size;
@@ -644,7 +666,7 @@ extern "C" pkv_status pkv_paged_decode_attn(const pkv_bf16 *q, const pkv_bf16 *k
         return PKV_EINVAL;
     if (num_pages * page_size > 0x7fffffffll) return PKV_EUNSUPPORTED;
     // total tiles must fit the block's int32 prefix sums
-    const int T = head_dim == 128 ? Shape<128>::T : Shape<64>::T;
+    const int T = head_dim == 128 ? Shape<128, 1>::T : Shape<64, 1>::T;  // T depends on head_dim only
     const int64_t max_tiles = (page_table_stride * page_size + T - 1) / T;
     if (static_cast<double>(batch) * num_kv_heads * max_tiles >= 2147483647.0)
         return PKV_EUNSUPPORTED;
