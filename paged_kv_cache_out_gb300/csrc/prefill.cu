@@ -71,7 +71,8 @@ struct Layout {
     static constexpr int OFF_V = OFF_K + kKStages * KV_BYTES;
     static constexpr int OFF_BAR = OFF_V + kVStages * KV_BYTES;
     // qfull, kfull/kempty[kKStages], vfull/vempty[kVStages], per query tile: sfull, pfull, odone
-    static constexpr int NBARS = 1 + 2 * kKStages + 2 * kVStages + NQ * 3;
+    // + per query tile: turn (its softmax finished a key tile)
+    static constexpr int NBARS = 1 + 2 * kKStages + 2 * kVStages + NQ * 4;
     static constexpr int OFF_MISC = OFF_BAR + NBARS * 8;
     static constexpr int TOTAL = OFF_MISC + 64;
     // at least 116 KB: one block per SM (it holds all 512 TMEM columns)
@@ -171,9 +172,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto B_VFULL = [](int s) { return 1 + 2 * kKStages + s; };
     auto B_VEMPTY = [](int s) { return 1 + 2 * kKStages + kVStages + s; };
     constexpr int kTileBar0 = 1 + 2 * kKStages + 2 * kVStages;
-    auto B_SFULL = [](int qt) { return kTileBar0 + qt * 3; };
-    auto B_PFULL = [](int qt) { return kTileBar0 + qt * 3 + 1; };
-    auto B_ODONE = [](int qt) { return kTileBar0 + qt * 3 + 2; };
+    auto B_SFULL = [](int qt) { return kTileBar0 + qt * 4; };
+    auto B_PFULL = [](int qt) { return kTileBar0 + qt * 4 + 1; };
+    auto B_ODONE = [](int qt) { return kTileBar0 + qt * 4 + 2; };
+    auto B_TURN = [](int qt) { return kTileBar0 + qt * 4 + 3; };
     volatile int *misc = reinterpret_cast<volatile int *>(smem + Lo::OFF_MISC);
     volatile int *abort_flag = misc + 0;
     volatile int *bad_page = misc + 1;
@@ -193,6 +195,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(BAR(B_SFULL(qt)), 1);
             mbar_init(BAR(B_PFULL(qt)), 4);
             mbar_init(BAR(B_ODONE(qt)), 1);
+            mbar_init(BAR(B_TURN(qt)), 4);
         }
         *abort_flag = 0;
         *bad_page = 0;
@@ -421,6 +424,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             // S(j) complete implies PV(j-1) complete: O is stable and P free
             ok = mbar_wait_warp(BAR(B_SFULL(qt)), j & 1, abort_flag, dev_status);
             if (!ok) break;
+            // The two softmax warpgroups take turns (A(0), B(0), A(1), B(1), ...)
+            // so that one's exponentials always overlap the other's MMAs instead
+            // of both competing for the same SM sub-partitions at once.
+            if (qt == 0 ? (j >= 1 && j - 1 < nkt[1]) : (j < nkt[0])) {
+                const int other = 1 - qt;
+                const int done = qt == 0 ? j - 1 : j;  // key tile the other group must have finished
+                ok = mbar_wait_warp(BAR(B_TURN(other)), done & 1, abort_flag, dev_status);
+                if (!ok) break;
+            }
             tc_fence_after();
             // all 128 scores of this row in registers (one wait for four loads)
             uint32_t sv[BN];
@@ -487,7 +499,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_wait_st();  // P and O stores
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(BAR(B_PFULL(qt)));
+            if (lane == 0) {
+                mbar_arrive(BAR(B_PFULL(qt)));
+                mbar_arrive(BAR(B_TURN(qt)));
+            }
         }
         if (ok && my_kt > 0) ok = mbar_wait_warp(BAR(B_ODONE(qt)), (my_kt - 1) & 1, abort_flag, dev_status);
         tc_fence_after();
