@@ -277,6 +277,25 @@ def run_gpu(args, rank, world):
     e2e_ms = reduce_max(e0.elapsed_time(e1) / args.steps, world)
     assert int(status.item()) == 0
 
+    # ---- the same step through the fused entry point (kv_store inside decode)
+    def fused_step():
+        pkv.paged_decode_attn_store(q, k_new, v_new, out_loc, k, v, pt, sl, x.scale, workspace=ws,
+                                    dev_status=status, out=out, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            fused_step()
+        stream.synchronize()
+        barrier()
+        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        f0.record(stream)
+        for _ in range(args.steps):
+            fused_step()
+        f1.record(stream)
+    stream.synchronize()
+    fused_ms = reduce_max(f0.elapsed_time(f1) / args.steps, world)
+    assert int(status.item()) == 0
+
     # ---- prefill TFLOP/s on the ragged-prefill workload, the long-context decode
     # and the mixed continuous-batching step (rank 0 reports)
     prefill = long_dec = mixed = None
@@ -331,6 +350,12 @@ def run_gpu(args, rank, world):
             "ms_per_step": round(e2e_ms, 5),
             "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h,
+        },
+        "fused_step": {
+            "entry": "pkv_paged_decode_attn_store (kv_store fused into decode, 2 launches)",
+            "value": round(world * B_step / (fused_ms * 1e-3) / 1e9, 2),
+            "unit": "GB/s",
+            "ms_per_step": round(fused_ms, 5),
         },
         "gpu_launches": 3 * args.steps,
         "clocks": clocks.summary(),

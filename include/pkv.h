@@ -5,6 +5,8 @@
  *
  *   pkv_kv_store            write this step's new K/V rows into their pool slots
  *   pkv_paged_decode_attn   one query token per sequence over its cached keys
+ *   pkv_paged_decode_attn_store  kv_store of the decode rows fused into the
+ *                           decode attention (one launch instead of two)
  *   pkv_paged_prefill_attn  ragged causal attention of new tokens over a
  *                           cached prefix plus themselves
  *
@@ -149,6 +151,44 @@ pkv_status pkv_paged_decode_attn(const pkv_bf16 *q, const pkv_bf16 *k_cache,
                                  float softmax_scale, void *workspace,
                                  size_t workspace_bytes, int32_t *dev_status,
                                  pkv_bf16 *out, void *stream);
+
+/*
+ * paged_decode_attn_store: pkv_kv_store of each sequence's one new K/V row
+ * followed by pkv_paged_decode_attn, in one call (two kernels instead of
+ * three).
+ *
+ * mini-sglang "Engine Class": in a decode batch each request brings one new
+ * token whose K/V row is written to the cache slot out_loc names and which
+ * its own query attends to; miniVLLM "Engine Architecture", prepare_decode:
+ * slot_mapping holds the slot of each sequence's last position.
+ *
+ *   k_new, v_new  [batch, num_kv_heads, head_dim] bf16, read: the new rows
+ *   out_loc       [batch] int32: the pool slot of sequence b's new row, which
+ *                 must be the slot position seq_lens[b] - 1 maps to; < 0
+ *                 skips the store (that position is then read from the pool
+ *                 as it is)
+ *   k_cache, v_cache  the pool, written at the out_loc slots bit for bit as
+ *                 pkv_kv_store writes them, then read as by
+ *                 pkv_paged_decode_attn
+ *   out           exactly as kv_store followed by pkv_paged_decode_attn
+ *   other arguments, workspace and limits as for pkv_paged_decode_attn.
+ * Each row is stored by the thread block that reads the tile holding position
+ * seq_lens[b] - 1 of that sequence, before it reads that tile.  Device errors
+ * add to those of pkv_paged_decode_attn: PKV_DEV_BAD_SLOT when out_loc[b] is
+ * >= num_pages * page_size (row not stored), or is not the slot of position
+ * seq_lens[b] - 1 (row stored; blocks that read that slot in the same call may
+ * see either value, so the outputs are unspecified).  A sequence with
+ * seq_lens[b] == 0 still has its row stored and gets a zero output.
+ */
+pkv_status pkv_paged_decode_attn_store(const pkv_bf16 *q, const pkv_bf16 *k_new,
+                                       const pkv_bf16 *v_new, const int32_t *out_loc,
+                                       pkv_bf16 *k_cache, pkv_bf16 *v_cache,
+                                       const int32_t *page_table, int64_t page_table_stride,
+                                       const int32_t *seq_lens, int batch, int num_q_heads,
+                                       int num_kv_heads, int head_dim, int page_size,
+                                       int64_t num_pages, float softmax_scale,
+                                       void *workspace, size_t workspace_bytes,
+                                       int32_t *dev_status, pkv_bf16 *out, void *stream);
 
 /*
  * paged_prefill_attn: causal attention of each request's new tokens over its

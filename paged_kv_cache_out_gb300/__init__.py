@@ -15,5 +15,6 @@ from .binding import (  # noqa: F401
     kv_store,
     load_library,
     paged_decode_attn,
+    paged_decode_attn_store,
     paged_prefill_attn,
 )

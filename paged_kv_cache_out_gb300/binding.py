@@ -31,6 +31,8 @@ SIGNATURES = {
     "pkv_decode_workspace_size": ([_I32, _I32, _I32, _I32], _SZ),
     "pkv_paged_decode_attn": ([_P, _P, _P, _P, _I64, _P, _I32, _I32, _I32, _I32, _I32, _I64,
                                _F32, _P, _SZ, _P, _P, _P], _I32),
+    "pkv_paged_decode_attn_store": ([_P, _P, _P, _P, _P, _P, _P, _I64, _P, _I32, _I32, _I32,
+                                     _I32, _I32, _I64, _F32, _P, _SZ, _P, _P, _P], _I32),
     "pkv_paged_prefill_attn": ([_P, _P, _P, _P, _P, _I64, _P, _I32, _I64, _I32, _I32, _I32,
                                 _I32, _I32, _I64, _F32, _P, _P, _P], _I32),
     "pkv_paged_decode_attn_noalloc": ([_P, _P, _P, _P, _I64, _P, _I32, _I32, _I32, _I32, _I32,
@@ -129,6 +131,34 @@ def paged_decode_attn(q, k_cache, v_cache, page_table, seq_lens, softmax_scale, 
         _ptr(seq_lens), B, Hq, Hkv, d, ps, P, float(softmax_scale), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _ptr(dev_status), _ptr(out), _stream(stream))
     _check("pkv_paged_decode_attn", st)
+    return out
+
+
+def paged_decode_attn_store(q, k_new, v_new, out_loc, k_cache, v_cache, page_table, seq_lens,
+                            softmax_scale, workspace=None, dev_status=None, out=None, stream=None):
+    """kv_store of the decode rows k_new/v_new [B, Hkv, d] at out_loc [B] fused
+    into decode attention (same results as kv_store followed by paged_decode_attn)."""
+    for t, n in ((q, "q"), (k_new, "k_new"), (v_new, "v_new"), (k_cache, "k_cache"),
+                 (v_cache, "v_cache")):
+        _bf16(t, n)
+    _i32(seq_lens, "seq_lens"), _i32(out_loc, "out_loc")
+    if page_table.dtype != torch.int32 or page_table.dim() != 2 or page_table.stride(1) != 1:
+        raise ValueError("page_table must be a 2-D int32 tensor with unit column stride")
+    B, Hq, d = q.shape
+    P, ps, Hkv, d2 = k_cache.shape
+    if (d2 != d or v_cache.shape != k_cache.shape or seq_lens.shape[0] != B
+            or out_loc.shape[0] != B or k_new.shape != (B, Hkv, d) or v_new.shape != (B, Hkv, d)):
+        raise ValueError("shape mismatch")
+    if out is None:
+        out = torch.empty_like(q)
+    if workspace is None:
+        workspace = decode_workspace(B, Hq, Hkv, d, q.device)
+    st = load_library().pkv_paged_decode_attn_store(
+        _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(out_loc), _ptr(k_cache), _ptr(v_cache),
+        _ptr(page_table), page_table.stride(0), _ptr(seq_lens), B, Hq, Hkv, d, ps, P,
+        float(softmax_scale), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _ptr(dev_status), _ptr(out), _stream(stream))
+    _check("pkv_paged_decode_attn_store", st)
     return out
 
 

@@ -120,6 +120,12 @@ __device__ __forceinline__ uint64_t l2_evict_last_policy() {
     return pol;
 }
 
+// Order this thread's generic-proxy global writes before its (and, after a
+// barrier, its peers') later copy-engine reads of global memory.
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }

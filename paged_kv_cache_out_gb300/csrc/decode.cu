@@ -65,7 +65,7 @@ struct Smem {
     static constexpr int RING = S::STAGES * STAGE_BYTES;
     static constexpr int RED_O = S::GROUPS * G * D * 4;
     static constexpr int RED_ML = S::GROUPS * G * 2 * 4;
-    static constexpr int BARS = 2 * S::STAGES * 8;
+    static constexpr int BARS = (2 * S::STAGES + 1) * 8;  // full, empty, fused stores done
     static constexpr int FLAGS = S::STAGES * 4 + 16;
     static constexpr int FIXED = RING + RED_O + RED_ML + BARS + FLAGS;
     // + tile offsets [batch + 1] and sequence lengths [batch], int32
@@ -101,6 +101,7 @@ __device__ __forceinline__ int owner_search(const int32_t *prefix, int B, int64_
 struct Piece {
     int b, g;
     int t0, t1;         // tile range inside the segment
+    int nt;             // tiles of the whole segment
     bool whole;         // covers the whole segment
     bool block_first;   // first piece of this block
 };
@@ -117,6 +118,7 @@ __device__ __forceinline__ bool next_piece(int64_t &pos, int64_t end, int64_t bl
     const int64_t seg_end = prefix[b] + (int64_t)(p.g + 1) * nt;
     const int64_t pend = end < seg_end ? end : seg_end;
     p.t1 = p.t0 + static_cast<int>(pend - pos);
+    p.nt = nt;
     p.whole = (p.t0 == 0) && (pend == seg_end);
     p.block_first = (pos == block_start);
     pos = pend;
@@ -167,14 +169,94 @@ __device__ void build_prefix(int32_t *prefix, int32_t *lens, const int32_t *seq_
     __syncthreads();
 }
 
-template <int D, int G>
+// The fused store: each sequence's new K/V row (k_new/v_new [B, Hkv, D]) is
+// written to pool slot out_loc[b], which must be the slot of position
+// seq_lens[b] - 1.  k_new == nullptr turns it off.
+struct Fuse {
+    const __nv_bfloat16 *k_new;
+    const __nv_bfloat16 *v_new;
+    const int32_t *out_loc;
+    __nv_bfloat16 *k_cache;
+    __nv_bfloat16 *v_cache;
+};
+
+// Copy one head's new K and V rows (D bf16 each) to their pool slot with the
+// lanes of one warp.
+template <int D>
+__device__ __forceinline__ void store_new_rows(const Fuse &fz, int b, int g, int Hkv, int64_t slot,
+                                               int lane) {
+    constexpr int VEC = D * 2 / 16;
+    const uint4 *ks = reinterpret_cast<const uint4 *>(fz.k_new + ((int64_t)b * Hkv + g) * D);
+    const uint4 *vs = reinterpret_cast<const uint4 *>(fz.v_new + ((int64_t)b * Hkv + g) * D);
+    uint4 *kd = reinterpret_cast<uint4 *>(fz.k_cache + (slot * Hkv + g) * D);
+    uint4 *vd = reinterpret_cast<uint4 *>(fz.v_cache + (slot * Hkv + g) * D);
+    for (int i = lane; i < VEC; i += 32) {
+        kd[i] = __ldg(ks + i);
+        vd[i] = __ldg(vs + i);
+    }
+}
+
+// Fused store, run by the consumer threads of a block before its first tile:
+// every segment (b, g) whose last tile lies in the block's range [t0, t1) gets
+// its new K/V row written to pool slot out_loc[b], one thread per segment.
+// Those segments are consecutive in (b, g) order.  Ends with a proxy fence, so
+// that after the barrier that follows, the copy engine reads the stored rows.
+template <int D>
+__device__ void store_block_rows(const Fuse &fz, const int32_t *prefix, const int32_t *lens,
+                                 const int32_t *page_table, int64_t pt_stride, int B, int Hkv,
+                                 int ps_log2, int64_t num_slots, int64_t t0, int64_t t1, int ctid,
+                                 int32_t *dev_status) {
+    constexpr int CH = D * 2 / 16;  // 16-byte chunks of a row
+    const int b0 = owner_search(prefix, B, t0);
+    const int b1 = owner_search(prefix, B, t1 - 1);
+    const int64_t o0 = (int64_t)b0 * Hkv + (t0 - prefix[b0]) / ((prefix[b0 + 1] - prefix[b0]) / Hkv);
+    const int64_t o1 = (int64_t)b1 * Hkv + (t1 - 1 - prefix[b1]) / ((prefix[b1 + 1] - prefix[b1]) / Hkv);
+    bool flag = false;
+    for (int64_t o = o0 + ctid; o <= o1; o += kConsumerWarps * 32) {
+        const int b = static_cast<int>(o / Hkv), g = static_cast<int>(o % Hkv);
+        const int nt = (prefix[b + 1] - prefix[b]) / Hkv;
+        if (nt == 0) continue;  // no keys: the merge kernel stores its row
+        const int64_t last = prefix[b] + (int64_t)(g + 1) * nt - 1;
+        if (last < t0 || last >= t1) continue;
+        const int64_t slot = fz.out_loc[b];
+        if (slot < 0) continue;
+        if (slot >= num_slots) {
+            flag = true;  // beyond the pool: not stored
+            continue;
+        }
+        const int L = lens[b];
+        const int64_t expect =
+            ((int64_t)page_table[(int64_t)b * pt_stride + ((L - 1) >> ps_log2)] << ps_log2) +
+            ((L - 1) & ((1 << ps_log2) - 1));
+        if (slot != expect) flag = true;
+        const uint4 *ks = reinterpret_cast<const uint4 *>(fz.k_new + ((int64_t)b * Hkv + g) * D);
+        const uint4 *vs = reinterpret_cast<const uint4 *>(fz.v_new + ((int64_t)b * Hkv + g) * D);
+        uint4 *kd = reinterpret_cast<uint4 *>(fz.k_cache + (slot * Hkv + g) * D);
+        uint4 *vd = reinterpret_cast<uint4 *>(fz.v_cache + (slot * Hkv + g) * D);
+        uint4 kr[CH], vr[CH];
+#pragma unroll
+        for (int c = 0; c < CH; ++c) {
+            kr[c] = __ldg(ks + c);
+            vr[c] = __ldg(vs + c);
+        }
+#pragma unroll
+        for (int c = 0; c < CH; ++c) {
+            kd[c] = kr[c];
+            vd[c] = vr[c];
+        }
+    }
+    if (flag && dev_status) atomicOr(dev_status, PKV_DEV_BAD_SLOT);
+    fence_proxy_async_global();
+}
+
+template <int D, int G, bool FUSE>
 __global__ void __launch_bounds__(kThreads, G <= 4 ? kCtasPerSm : 1)
     decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                   const __nv_bfloat16 *__restrict__ q, const int32_t *__restrict__ page_table,
                   int64_t pt_stride, const int32_t *__restrict__ seq_lens, int B, int Hkv,
                   int ps_log2, int box_rows, int64_t num_pages, float scale_log2,
                   float *__restrict__ ws_part, int32_t *__restrict__ ws_prefix,
-                  int32_t *dev_status, __nv_bfloat16 *__restrict__ out) {
+                  int32_t *dev_status, __nv_bfloat16 *__restrict__ out, const Fuse fz) {
     using S = Shape<D, G>;
     using M = Smem<D, G>;
     constexpr int T = S::T, R = S::R, U = S::U, GROUPS = S::GROUPS, STAGES = S::STAGES;
@@ -202,6 +284,7 @@ __global__ void __launch_bounds__(kThreads, G <= 4 ? kCtasPerSm : 1)
             mbar_init(smem_u32(&bars[s]), 1);                        // full: producer + tx bytes
             mbar_init(smem_u32(&bars[STAGES + s]), kConsumerWarps);  // empty: one per consumer warp
         }
+        mbar_init(smem_u32(&bars[2 * STAGES]), kConsumerWarps);  // fused stores written
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -229,6 +312,7 @@ __global__ void __launch_bounds__(kThreads, G <= 4 ? kCtasPerSm : 1)
         Piece p;
         uint32_t it = 0;
         bool ok = true;
+        bool stores_seen = false;
         // boxes per tile; up to 32 of them page ids come in warp-wide windows
         // of 32 boxes, the next window loaded one window ahead
         const int bpt = T / box_rows;
@@ -280,6 +364,16 @@ __global__ void __launch_bounds__(kThreads, G <= 4 ? kCtasPerSm : 1)
                 }
                 bad = __any_sync(0xffffffffu, bad);
                 const bool first = (tile == p.t0);
+                // fused store: the consumers write the new rows of the block's
+                // segments first; a segment's last tile (which holds its new
+                // row) is copied only after that
+                if (FUSE && tile == p.nt - 1 && !stores_seen) {
+                    if (!mbar_wait_warp(smem_u32(&bars[2 * STAGES]), 0, abort_flag, dev_status)) {
+                        ok = false;
+                        break;
+                    }
+                    stores_seen = true;
+                }
                 const uint32_t bytes = (bad ? 0u : 2u * box_bytes * nbox) +
                                        (first ? static_cast<uint32_t>(G * D * 2) : 0u);
                 uint8_t *st = ring + s * M::STAGE_BYTES;
@@ -316,6 +410,14 @@ __global__ void __launch_bounds__(kThreads, G <= 4 ? kCtasPerSm : 1)
     const int lr = lane % R;                             // slice of a row
     // the lane owns 16-byte chunks lr, lr + R, ... of each row
     const int ctid = tid;                                // 0..127
+    if constexpr (FUSE) {
+        // while the first tiles are in flight: store the new K/V rows of the
+        // segments whose last tile is in this block, then tell the producer
+        store_block_rows<D>(fz, prefix, lens, page_table, pt_stride, B, Hkv, ps_log2,
+                            num_pages << ps_log2, my_start, my_end, ctid, dev_status);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&bars[2 * STAGES]));
+    }
     // q (pre-scaled by scale*log2 e) and the output slice as fp32 pairs, so the
     // dot products and the value accumulation run as packed fp32x2 FMAs
     float2 q2[G][4 * NCH];
@@ -504,7 +606,8 @@ template <int D, int G>
 __global__ void __launch_bounds__(128)
     decode_merge_kernel(const int32_t *__restrict__ seq_lens, const int32_t *__restrict__ ws_prefix,
                         const float *__restrict__ ws_part, int B, int Hkv, int64_t cap, int grid,
-                        int32_t *dev_status, __nv_bfloat16 *__restrict__ out) {
+                        int32_t *dev_status, __nv_bfloat16 *__restrict__ out, const Fuse fz,
+                        int64_t num_slots) {
     using S = Shape<D, G>;
     grid_dependency_wait();  // partial states come from the main kernel
     const int b = blockIdx.x / Hkv, g = blockIdx.x % Hkv;
@@ -514,6 +617,14 @@ __global__ void __launch_bounds__(128)
     if (nt == 0) {
         const int L = seq_lens[b];
         const bool bad = (L < 0 || L > cap);
+        // fused store of a sequence that attends to nothing: still store its row
+        if (fz.k_new && threadIdx.x < 32) {
+            const int64_t slot = fz.out_loc[b];
+            if (slot >= 0 && slot < num_slots)
+                store_new_rows<D>(fz, b, g, Hkv, slot, threadIdx.x);
+            else if (slot >= num_slots && threadIdx.x == 0 && dev_status)
+                atomicOr(dev_status, PKV_DEV_BAD_SLOT);
+        }
         if (bad && g == 0 && threadIdx.x == 0 && dev_status) atomicOr(dev_status, PKV_DEV_BAD_SEQLEN);
         for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x)
             orow[idx] = __float2bfloat16_rn(bad ? __int_as_float(0x7fc00000) : 0.f);
@@ -566,11 +677,15 @@ static bool prepare(const pkv_host::DeviceInfo &dev, int batch, int *ctas_per_sm
     const size_t max_smem = Smem<D, G>::bytes(kMaxBatch);
     if (!li.ready) {
         if (max_smem > static_cast<size_t>(dev.max_smem_optin)) return false;
-        if (cudaFuncSetAttribute(decode_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(decode_kernel<D, G, false>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(max_smem)) != cudaSuccess ||
+            cudaFuncSetAttribute(decode_kernel<D, G, true>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(max_smem)) != cudaSuccess)
             return false;
         int n = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel<D, G>, kThreads,
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel<D, G, false>, kThreads,
                                                           Smem<D, G>::bytes(256)) != cudaSuccess)
             return false;
         li.ctas_per_sm = n < 1 ? 1 : (n > kCtasPerSm ? kCtasPerSm : n);
@@ -585,7 +700,7 @@ template <int D, int G>
 static pkv_status launch(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf16 *v_cache,
                          const int32_t *page_table, int64_t pt_stride, const int32_t *seq_lens,
                          int B, int Hkv, int page_size, int64_t num_pages, float scale,
-                         void *workspace, int32_t *dev_status, pkv_bf16 *out,
+                         void *workspace, int32_t *dev_status, pkv_bf16 *out, const Fuse &fz,
                          cudaStream_t stream) {
     pkv_host::DeviceInfo dev;
     if (!pkv_host::current_device(&dev)) return PKV_ECUDA;
@@ -605,18 +720,20 @@ static pkv_status launch(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_b
     float *ws_part = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) +
                                                (((size_t)(B + 1) * 4 + 255) & ~size_t(255)));
     const float scale_log2 = scale * kLog2e;
-    if (pkv_host::launch_dependent(decode_kernel<D, G>, dim3(grid), dim3(kThreads),
+    // the fused store has its own instantiation, so the plain call carries none of it
+    auto kernel = fz.k_new ? decode_kernel<D, G, true> : decode_kernel<D, G, false>;
+    if (pkv_host::launch_dependent(kernel, dim3(grid), dim3(kThreads),
                                    Smem<D, G>::bytes(B), stream, kmap, vmap,
                                    reinterpret_cast<const __nv_bfloat16 *>(q), page_table, pt_stride,
                                    seq_lens, B, Hkv, ps_log2, box_rows, num_pages, scale_log2,
                                    ws_part, ws_prefix, dev_status,
-                                   reinterpret_cast<__nv_bfloat16 *>(out)) != cudaSuccess)
+                                   reinterpret_cast<__nv_bfloat16 *>(out), fz) != cudaSuccess)
         return PKV_ECUDA;
     if (pkv_host::launch_dependent(decode_merge_kernel<D, G>, dim3(B * Hkv), dim3(128), 0, stream,
                                    seq_lens, static_cast<const int32_t *>(ws_prefix),
                                    static_cast<const float *>(ws_part), B, Hkv,
                                    pt_stride * page_size, grid, dev_status,
-                                   reinterpret_cast<__nv_bfloat16 *>(out)) != cudaSuccess)
+                                   reinterpret_cast<__nv_bfloat16 *>(out), fz, slots) != cudaSuccess)
         return PKV_ECUDA;
     return PKV_OK;
 }
@@ -641,14 +758,13 @@ extern "C" size_t pkv_decode_workspace_size(int batch, int num_q_heads, int num_
     return prefix + grid * 2 * (static_cast<size_t>(G) * head_dim + 2 * G) * 4;
 }
 
-extern "C" pkv_status pkv_paged_decode_attn(const pkv_bf16 *q, const pkv_bf16 *k_cache,
-                                            const pkv_bf16 *v_cache, const int32_t *page_table,
-                                            int64_t page_table_stride, const int32_t *seq_lens,
-                                            int batch, int num_q_heads, int num_kv_heads,
-                                            int head_dim, int page_size, int64_t num_pages,
-                                            float softmax_scale, void *workspace,
-                                            size_t workspace_bytes, int32_t *dev_status,
-                                            pkv_bf16 *out, void *stream) {
+// Shared argument checks and dispatch of the plain and the fused entry points.
+static pkv_status decode_entry(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf16 *v_cache,
+                               const int32_t *page_table, int64_t page_table_stride,
+                               const int32_t *seq_lens, int batch, int num_q_heads,
+                               int num_kv_heads, int head_dim, int page_size, int64_t num_pages,
+                               float softmax_scale, void *workspace, size_t workspace_bytes,
+                               int32_t *dev_status, pkv_bf16 *out, const Fuse &fz, void *stream) {
     if (batch < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_pages <= 0 ||
         page_table_stride < 0 || page_size <= 0)
         return PKV_EINVAL;
@@ -664,6 +780,8 @@ extern "C" pkv_status pkv_paged_decode_attn(const pkv_bf16 *q, const pkv_bf16 *k
     if (!pkv_host::aligned16(q) || !pkv_host::aligned16(k_cache) || !pkv_host::aligned16(v_cache) ||
         !pkv_host::aligned16(out) || !pkv_host::aligned16(workspace))
         return PKV_EINVAL;
+    if (fz.k_new && (!pkv_host::aligned16(fz.k_new) || !pkv_host::aligned16(fz.v_new)))
+        return PKV_EINVAL;
     if (num_pages * page_size > 0x7fffffffll) return PKV_EUNSUPPORTED;
     // total tiles must fit the block's int32 prefix sums
     const int T = head_dim == 128 ? Shape<128, 1>::T : Shape<64, 1>::T;  // T depends on head_dim only
@@ -677,7 +795,7 @@ extern "C" pkv_status pkv_paged_decode_attn(const pkv_bf16 *q, const pkv_bf16 *k
     if (head_dim == DD && G == GG)                                                              \
         return launch<DD, GG>(q, k_cache, v_cache, page_table, page_table_stride, seq_lens, batch, \
                               num_kv_heads, page_size, num_pages, softmax_scale, workspace,     \
-                              dev_status, out, st);
+                              dev_status, out, fz, st);
     PKV_DECODE_CASE(128, 1)
     PKV_DECODE_CASE(128, 2)
     PKV_DECODE_CASE(128, 4)
@@ -688,4 +806,34 @@ extern "C" pkv_status pkv_paged_decode_attn(const pkv_bf16 *q, const pkv_bf16 *k
     PKV_DECODE_CASE(64, 8)
 #undef PKV_DECODE_CASE
     return PKV_EUNSUPPORTED;
+}
+
+extern "C" pkv_status pkv_paged_decode_attn(const pkv_bf16 *q, const pkv_bf16 *k_cache,
+                                            const pkv_bf16 *v_cache, const int32_t *page_table,
+                                            int64_t page_table_stride, const int32_t *seq_lens,
+                                            int batch, int num_q_heads, int num_kv_heads,
+                                            int head_dim, int page_size, int64_t num_pages,
+                                            float softmax_scale, void *workspace,
+                                            size_t workspace_bytes, int32_t *dev_status,
+                                            pkv_bf16 *out, void *stream) {
+    const Fuse none{nullptr, nullptr, nullptr, nullptr, nullptr};
+    return decode_entry(q, k_cache, v_cache, page_table, page_table_stride, seq_lens, batch,
+                        num_q_heads, num_kv_heads, head_dim, page_size, num_pages, softmax_scale,
+                        workspace, workspace_bytes, dev_status, out, none, stream);
+}
+
+extern "C" pkv_status pkv_paged_decode_attn_store(
+    const pkv_bf16 *q, const pkv_bf16 *k_new, const pkv_bf16 *v_new, const int32_t *out_loc,
+    pkv_bf16 *k_cache, pkv_bf16 *v_cache, const int32_t *page_table, int64_t page_table_stride,
+    const int32_t *seq_lens, int batch, int num_q_heads, int num_kv_heads, int head_dim,
+    int page_size, int64_t num_pages, float softmax_scale, void *workspace,
+    size_t workspace_bytes, int32_t *dev_status, pkv_bf16 *out, void *stream) {
+    if (batch > 0 && (!k_new || !v_new || !out_loc)) return PKV_EINVAL;
+    const Fuse fz{reinterpret_cast<const __nv_bfloat16 *>(k_new),
+                  reinterpret_cast<const __nv_bfloat16 *>(v_new), out_loc,
+                  reinterpret_cast<__nv_bfloat16 *>(k_cache),
+                  reinterpret_cast<__nv_bfloat16 *>(v_cache)};
+    return decode_entry(q, k_cache, v_cache, page_table, page_table_stride, seq_lens, batch,
+                        num_q_heads, num_kv_heads, head_dim, page_size, num_pages, softmax_scale,
+                        workspace, workspace_bytes, dev_status, out, fz, stream);
 }
