@@ -511,7 +511,7 @@ def time_mixed_step(args, dev, stream):
             "ms_per_step_eager": round(eager_ms, 4), "ms_per_step_graph": round(graph_ms, 4),
             "tokens_per_s": round(x.Tq / (graph_ms * 1e-3), 1),
             "decode_plus_store_gbs": round(nbytes / (graph_ms * 1e-3) / 1e9, 1),
-            "prefill_flops_per_step": fl, "launches_per_step": 5 * layers}
+            "prefill_flops_per_step": fl, "launches_per_step": 4 * layers}
 
 
 def reduce_max(v, world):
