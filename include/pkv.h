@@ -210,6 +210,11 @@ pkv_status pkv_paged_decode_attn_store(const pkv_bf16 *q, const pkv_bf16 *k_new,
  *                 request r (absolute position c_r + i) attends keys
  *                 0 .. c_r + i; accumulated in fp32, rounded to bf16
  * Other arguments as for pkv_paged_decode_attn.
+ * The kernel is persistent (one thread block per SM) and hands out its work
+ * through a counter pair that the library keeps in device memory: each call
+ * takes the next of 256 pairs, and its last block resets the pair.  So at
+ * most 256 calls may run at the same time, and a call captured in a CUDA
+ * graph keeps its pair: one captured call must not run twice at once.
  */
 pkv_status pkv_paged_prefill_attn(const pkv_bf16 *q, const int32_t *cu_seqlens_q,
                                   const pkv_bf16 *k_cache, const pkv_bf16 *v_cache,

@@ -81,6 +81,31 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     }
 }
 
+// Wait until the shared-memory counter *cnt reaches target (a scheduling wait
+// between warps of one block, polled with short sleeps).  Gives up like
+// mbar_wait.  Warp-uniform outcome.
+__device__ __forceinline__ bool wait_count(const int *cnt, int target, volatile int *abort,
+                                           int32_t *dev_status) {
+    const volatile int *c = cnt;
+    bool ok = true;
+    if (*c < target) {
+        const uint64_t t0 = global_timer_ns();
+        for (uint32_t i = 1; *c < target; ++i) {
+            __nanosleep(32);
+            if ((i & 15) == 0) {
+                if (*abort) { ok = false; break; }
+                if (global_timer_ns() - t0 > kWaitLimitNs) {
+                    *abort = 1;
+                    if (dev_status) atomicOr(dev_status, PKV_DEV_TIMEOUT);
+                    ok = false;
+                    break;
+                }
+            }
+        }
+    }
+    return __all_sync(0xffffffffu, ok);
+}
+
 // The same wait taken by all 32 lanes of a warp, with one outcome for all of
 // them, so that warp-collective instructions after it are never divergent.
 __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int *abort,

@@ -9,15 +9,20 @@
 // 0 .. c_r + i (causal, aligned at the bottom right).  Grouped-query
 // attention shares one KV head among num_q_heads / num_kv_heads query heads.
 //
-// One block (one per SM) owns two 128-row query tiles, A and B, of one
-// request and one KV head; a tile holds 128/G consecutive new tokens x the G
-// query heads of that KV head, so every K/V tile staged in shared memory
-// serves 2 x 128 rows.  Roles (352 threads):
-//   warp 8      producer: Q tiles A and B once, then 128-key K and V tiles
-//               through 2-stage rings, K one tile ahead of V.  Pages of >= 8 tokens come in as TMA
-//               boxes (one per page and 64-column block, 128-byte swizzle,
-//               straight into the layout the tensor core reads); smaller
-//               pages are gathered by the warp's lanes with 16-byte loads and
+// Work item: two 128-row query tiles, A and B, of one request and one KV
+// head; a tile holds 128/G consecutive new tokens x the G query heads of that
+// KV head, so every K/V tile staged in shared memory serves 2 x 128 rows.
+// The kernel is persistent: one block per SM takes items from a queue (an
+// atomic counter) in order of decreasing work, heaviest first, so the last
+// items to finish are light ones, and the next item's Q and first K/V tiles
+// load while the current item finishes.  Roles (352 threads):
+//   warp 8      producer: takes the next item from the queue and publishes it
+//               to the other roles through a 2-slot ring; per item the Q
+//               tiles A and B, then 128-key K and V tiles through 2-stage
+//               rings, K one tile ahead of V.  Pages of >= 8 tokens come in as
+//               TMA boxes (one per page and 64-column block, 128-byte swizzle,
+//               straight into the layout the tensor core reads); smaller pages
+//               are gathered by the warp's lanes with 16-byte loads and
 //               swizzled stores.  Page ids are read in warp-wide windows, one
 //               window ahead.
 //   warps 9,10  warp 9 allocates all 512 TMEM columns (per query tile: a
@@ -36,12 +41,15 @@
 //               the causal mask by selection, keeps a running max and sum in
 //               the log2 domain, rescales its TMEM output row when the running
 //               max grew by more than 2^8 (exact: every term shares the
-//               reference), writes P into tensor memory, and at the end
-//               normalises and stores the row.
+//               reference), writes P into tensor memory, and at the end of the
+//               item reads O out of tensor memory (then frees it for the next
+//               item), normalises and stores the row.  A warp whose 32 rows
+//               are all past the request's last token does no arithmetic.
 // While one tile's softmax runs, the tensor core works on the other tile's PV
 // and QK^T.
 #include <math.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "common.cuh"
@@ -51,14 +59,23 @@ namespace prefill {
 
 constexpr int kThreads = 352;
 constexpr int BM = 128;  // rows of a query tile: (token, head) pairs
-constexpr int NQ = 2;    // query tiles per block
+constexpr int NQ = 2;    // query tiles per item
 constexpr int BN = 128;  // keys per KV tile
 constexpr int kKStages = 2, kVStages = 2;
 constexpr int kProducerWarp = 8, kMmaWarp = 9;  // warps 9 and 10 issue the MMAs of tiles A and B
+constexpr int kItemSlots = 2;                   // items published ahead of the consumers
+constexpr int kItemConsumers = 2 + 8;           // MMA warps + softmax warps
+constexpr int kRankGroups = kThreads;           // up to this many (token block, request) groups
+                                                // are ranked by work in the kernel
+constexpr int kSchedSlots = 256;                // queue counters for calls in flight at once
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kNegBig = -1.0e30f;
 constexpr float kRescaleLog2 = 8.0f;  // lazy rescale threshold (factor 256)
 constexpr uint32_t kTmemCols = 512;
+
+// Work-queue counters, one pair per slot: [0] next item, [1] blocks finished.
+// The last block of a call to finish puts both back to zero.
+static __device__ unsigned int g_sched[kSchedSlots][2];
 
 template <int D>
 struct Layout {
@@ -70,11 +87,13 @@ struct Layout {
     static constexpr int OFF_K = OFF_Q + NQ * Q_BYTES;
     static constexpr int OFF_V = OFF_K + kKStages * KV_BYTES;
     static constexpr int OFF_BAR = OFF_V + kVStages * KV_BYTES;
-    // qfull, kfull/kempty[kKStages], vfull/vempty[kVStages], per query tile: sfull, pfull, odone
-    // + per query tile: turn (its softmax finished a key tile)
-    static constexpr int NBARS = 1 + 2 * kKStages + 2 * kVStages + NQ * 4;
+    // qfull, qempty, kfull/kempty[kKStages], vfull/vempty[kVStages],
+    // per query tile: sfull, pfull, odone, ofree; item full/empty[kItemSlots]
+    static constexpr int NBARS = 2 + 2 * kKStages + 2 * kVStages + NQ * 4 + 2 * kItemSlots;
     static constexpr int OFF_MISC = OFF_BAR + NBARS * 8;
-    static constexpr int TOTAL = OFF_MISC + 64;
+    static constexpr int OFF_ITEMS = OFF_MISC + 64;     // decoded items, kItemSlots x 16 ints
+    static constexpr int OFF_RANK = OFF_ITEMS + kItemSlots * 64;  // int order[kRankGroups], weight[kRankGroups]
+    static constexpr int TOTAL = OFF_RANK + 2 * kRankGroups * 4;
     // at least 116 KB: one block per SM (it holds all 512 TMEM columns)
     static constexpr size_t bytes() { return TOTAL > 118784 ? TOTAL : 118784; }
 };
@@ -103,6 +122,55 @@ __device__ __forceinline__ uint32_t swz_offset(int row, int chunk16, int rows) {
     return static_cast<uint32_t>(blk * rows * 128 + row * 128 + ((c ^ (row & 7)) << 4));
 }
 
+// One work item: query tiles A and B of request r, token block mt, KV head g.
+struct Item {
+    int r, g, mt;
+    int cu0, n, L, c;
+    int tbeg[NQ], tend[NQ], nkt[NQ];
+    int n_kt;
+};
+
+template <int G>
+__device__ __forceinline__ void decode_item(int p, int Hkv, int B, int mtiles, const int *order,
+                                            bool ranked, const int32_t *cu_seqlens,
+                                            const int32_t *seq_lens, Item &it) {
+    constexpr int TOK = BM / G;
+    const int grank = p / Hkv;
+    it.g = p % Hkv;
+    const int grp = ranked ? order[grank] : grank;
+    it.mt = mtiles - 1 - grp / B;
+    it.r = grp % B;
+    it.cu0 = cu_seqlens[it.r];
+    it.n = cu_seqlens[it.r + 1] - it.cu0;
+    it.L = seq_lens[it.r];
+    it.c = it.L - it.n;
+    const int blk_tok0 = it.mt * NQ * TOK;
+#pragma unroll
+    for (int qt = 0; qt < NQ; ++qt) {
+        it.tbeg[qt] = blk_tok0 + qt * TOK;
+        it.tend[qt] = min(it.n, it.tbeg[qt] + TOK);
+        it.nkt[qt] = it.tend[qt] > it.tbeg[qt] ? (it.c + it.tend[qt] + BN - 1) / BN : 0;
+    }
+    it.n_kt = it.nkt[0] > it.nkt[1] ? it.nkt[0] : it.nkt[1];
+}
+
+// Work of a (token block, request) group in key tiles: 0 for no tokens, 1 for
+// invalid offsets or lengths (the producer only flags those).
+template <int G>
+__device__ __forceinline__ int group_weight(int grp, int B, int mtiles, int64_t Tq, int max_q_len,
+                                            int64_t cap, const int32_t *cu_seqlens,
+                                            const int32_t *seq_lens) {
+    constexpr int TOK = BM / G;
+    const int mt = mtiles - 1 - grp / B, r = grp % B;
+    const int cu0 = cu_seqlens[r], cu1 = cu_seqlens[r + 1];
+    const int n = cu1 - cu0, L = seq_lens[r];
+    if (cu0 < 0 || n < 0 || cu1 > Tq || (r == 0 && cu0 != 0) || n > max_q_len) return 1;
+    const int t0 = mt * NQ * TOK;
+    if (t0 >= n) return 0;
+    if (L - n < 0 || L > cap) return 1;
+    return (L - n + min(n, t0 + NQ * TOK) + BN - 1) / BN;
+}
+
 template <int D, int G>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
@@ -111,81 +179,52 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const int32_t *__restrict__ page_table, int64_t pt_stride,
                    const int32_t *__restrict__ seq_lens, int B, int64_t Tq, int max_q_len, int Hkv,
                    int ps_log2, int box_rows, int64_t num_pages, float scale_log2, int mtiles,
-                   int32_t *dev_status, __nv_bfloat16 *__restrict__ out) {
+                   unsigned int *sched, int32_t *dev_status, __nv_bfloat16 *__restrict__ out) {
     using Lo = Layout<D>;
     constexpr int TOK = BM / G;  // new tokens per query tile
     const int Hq = Hkv * G;
     const int64_t cap = pt_stride << ps_log2;
-
-    // ---- which tiles: heaviest (largest mt) first over all requests and heads
-    const int lin = blockIdx.x;
-    const int per_mt = B * Hkv;
-    const int mt = mtiles - 1 - lin / per_mt;
-    const int r = (lin % per_mt) / Hkv;
-    const int g = lin % Hkv;
-
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int cu0 = cu_seqlens[r], cu1 = cu_seqlens[r + 1];
-    const int n = cu1 - cu0;
-    const int L = seq_lens[r];
-    const int c = L - n;
-    const bool cu_bad = cu0 < 0 || n < 0 || cu1 > Tq || (r == 0 && cu0 != 0) || n > max_q_len;
-    if (cu_bad) {
-        if (tid == 0 && mt == 0 && g == 0 && dev_status) atomicOr(dev_status, PKV_DEV_BAD_CUSEQ);
-        return;
-    }
-    const int blk_tok0 = mt * NQ * TOK;
-    if (blk_tok0 >= n) return;
-    const int blk_tok1 = min(n, blk_tok0 + NQ * TOK);
-    const bool len_bad = (c < 0) || (L > cap);
-    if (len_bad) {
-        if (tid == 0 && mt == 0 && g == 0 && dev_status) atomicOr(dev_status, PKV_DEV_BAD_SEQLEN);
-        for (int idx = tid; idx < (blk_tok1 - blk_tok0) * G * D; idx += kThreads) {
-            const int t = blk_tok0 + idx / (G * D);
-            const int rem = idx % (G * D);
-            out[((int64_t)(cu0 + t) * Hq + (int64_t)g * G) * D + rem] =
-                __float2bfloat16_rn(__int_as_float(0x7fc00000));
-        }
-        return;
-    }
-    // per query tile: token range and number of 128-key tiles it needs
-    int tbeg[NQ], tend[NQ], nkt[NQ];
-#pragma unroll
-    for (int qt = 0; qt < NQ; ++qt) {
-        tbeg[qt] = blk_tok0 + qt * TOK;
-        tend[qt] = min(n, tbeg[qt] + TOK);
-        nkt[qt] = tend[qt] > tbeg[qt] ? (c + tend[qt] + BN - 1) / BN : 0;
-    }
-    const int n_kt = nkt[0] > nkt[1] ? nkt[0] : nkt[1];
 
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = smem_raw;
-    if (smem_u32(smem) & 1023u) {  // the 128-byte swizzle needs 1024-byte aligned tiles
-        if (tid == 0 && dev_status) atomicOr(dev_status, PKV_DEV_TIMEOUT);
-        return;
-    }
+    volatile int *misc = reinterpret_cast<volatile int *>(smem + Lo::OFF_MISC);
+    volatile int *abort_flag = misc + 0;
+    volatile int *item_ring = misc + 1;  // [kItemSlots]: published item, -1 = no more
+    volatile int *bad_flag = misc + 3;   // [kItemSlots]: a page id of that item was invalid
+    volatile int *n_items_s = misc + 5;
+    int *turn_cnt = const_cast<int *>(misc + 6);  // [NQ]: key-tile steps finished x 4 warps
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Lo::OFF_MISC + 32);
+    int *order = reinterpret_cast<int *>(smem + Lo::OFF_RANK);
+    Item *items = reinterpret_cast<Item *>(smem + Lo::OFF_ITEMS);  // the published items, decoded
+    int *weight = order + kRankGroups;
+
     const uint32_t bar0 = smem_u32(smem + Lo::OFF_BAR);
     auto BAR = [&](int i) -> uint32_t { return bar0 + 8u * i; };
-    const int B_QFULL = 0;
-    auto B_KFULL = [](int s) { return 1 + s; };
-    auto B_KEMPTY = [](int s) { return 1 + kKStages + s; };
-    auto B_VFULL = [](int s) { return 1 + 2 * kKStages + s; };
-    auto B_VEMPTY = [](int s) { return 1 + 2 * kKStages + kVStages + s; };
-    constexpr int kTileBar0 = 1 + 2 * kKStages + 2 * kVStages;
+    constexpr int B_QFULL = 0, B_QEMPTY = 1;
+    auto B_KFULL = [](int s) { return 2 + s; };
+    auto B_KEMPTY = [](int s) { return 2 + kKStages + s; };
+    auto B_VFULL = [](int s) { return 2 + 2 * kKStages + s; };
+    auto B_VEMPTY = [](int s) { return 2 + 2 * kKStages + kVStages + s; };
+    constexpr int kTileBar0 = 2 + 2 * kKStages + 2 * kVStages;
     auto B_SFULL = [](int qt) { return kTileBar0 + qt * 4; };
     auto B_PFULL = [](int qt) { return kTileBar0 + qt * 4 + 1; };
     auto B_ODONE = [](int qt) { return kTileBar0 + qt * 4 + 2; };
-    auto B_TURN = [](int qt) { return kTileBar0 + qt * 4 + 3; };
-    volatile int *misc = reinterpret_cast<volatile int *>(smem + Lo::OFF_MISC);
-    volatile int *abort_flag = misc + 0;
-    volatile int *bad_page = misc + 1;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Lo::OFF_MISC + 16);
+    auto B_OFREE = [](int qt) { return kTileBar0 + qt * 4 + 3; };
+    constexpr int kItemBar0 = kTileBar0 + NQ * 4;
+    auto B_IFULL = [](int s) { return kItemBar0 + s; };
+    auto B_IEMPTY = [](int s) { return kItemBar0 + kItemSlots + s; };
 
+    if (smem_u32(smem) & 1023u) {  // the 128-byte swizzle needs 1024-byte aligned tiles
+        if (tid == 0 && dev_status) atomicOr(dev_status, PKV_DEV_TIMEOUT);
+        return;  // uniform for the whole block, before any barrier or counter is touched
+    }
     if (tid == 0) {
         mbar_init(BAR(B_QFULL), 1);
+        mbar_init(BAR(B_QEMPTY), NQ);  // one commit per MMA warp
         for (int s = 0; s < kKStages; ++s) {
             mbar_init(BAR(B_KFULL(s)), 1);
-            mbar_init(BAR(B_KEMPTY(s)), NQ);  // released by both MMA warps
+            mbar_init(BAR(B_KEMPTY(s)), NQ);
         }
         for (int s = 0; s < kVStages; ++s) {
             mbar_init(BAR(B_VFULL(s)), 1);
@@ -195,20 +234,50 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(BAR(B_SFULL(qt)), 1);
             mbar_init(BAR(B_PFULL(qt)), 4);
             mbar_init(BAR(B_ODONE(qt)), 1);
-            mbar_init(BAR(B_TURN(qt)), 4);
+            mbar_init(BAR(B_OFREE(qt)), 4);
+        }
+        for (int s = 0; s < kItemSlots; ++s) {
+            mbar_init(BAR(B_IFULL(s)), 1);
+            mbar_init(BAR(B_IEMPTY(s)), kItemConsumers);
         }
         *abort_flag = 0;
-        *bad_page = 0;
+        *n_items_s = 0;
+        turn_cnt[0] = 0;
+        turn_cnt[1] = 0;
         fence_mbar_init();
     }
     if (warp == kMmaWarp) {
         tmem_alloc(smem_u32(tmem_slot), kTmemCols);
         tmem_relinquish();
     }
+    // Rank the (token block, request) groups by work, heaviest first, when
+    // there are few enough of them; all blocks compute the same order.
+    const int n_groups = mtiles * B;
+    const bool ranked = n_groups <= kRankGroups;
+    __syncthreads();  // n_items_s zeroed
+    if (ranked) {
+        if (tid < n_groups) {
+            const int w = group_weight<G>(tid, B, mtiles, Tq, max_q_len, cap, cu_seqlens, seq_lens);
+            weight[tid] = w;
+            if (w > 0) atomicAdd(const_cast<int *>(n_items_s), 1);
+        }
+        __syncthreads();
+        if (tid < n_groups) {
+            const int w = weight[tid];
+            int rank = 0;
+            for (int u = 0; u < n_groups; ++u) {
+                const int wu = weight[u];
+                rank += (wu > w) || (wu == w && u < tid);
+            }
+            order[rank] = tid;
+        }
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // groups of weight 0 are ranked last and never handed out
+    const int n_items = (ranked ? *n_items_s : n_groups) * Hkv;
     // TMEM columns: S (then P over its first 64 columns) of tile qt at 128 qt,
     // O of tile qt at 256 + 128 qt
     auto tm_s = [&](int qt) -> uint32_t { return tmem + qt * BN; };
@@ -217,122 +286,186 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t sQ = smem_u32(smem + Lo::OFF_Q);
     const uint32_t sK = smem_u32(smem + Lo::OFF_K);
     const uint32_t sV = smem_u32(smem + Lo::OFF_V);
-    const int32_t *prow = page_table + (int64_t)r * pt_stride;
 
     if (warp == kProducerWarp) {
         // ================================================================ producer
         const uint64_t pol_kv = l2_evict_last_policy();  // K/V tiles are re-read by other blocks
+        const uint64_t pol_q = l2_evict_first_policy();
         if (lane == 0) {
             prefetch_tmap(&qmap);
             if (box_rows >= 8) {
                 prefetch_tmap(&kmap);
                 prefetch_tmap(&vmap);
             }
-            mbar_arrive_expect_tx(BAR(B_QFULL), static_cast<uint32_t>(NQ * Lo::Q_BYTES));
-            const uint64_t pol_q = l2_evict_first_policy();
-#pragma unroll
-            for (int qt = 0; qt < NQ; ++qt)
-#pragma unroll
-                for (int blk = 0; blk < D / 64; ++blk)
-                    tma_load_3d(sQ + qt * Lo::Q_BYTES + blk * Lo::BLK, &qmap, BAR(B_QFULL), blk * 64,
-                                g * G, cu0 + tbeg[qt], pol_q);
         }
         const int ps_mask = (1 << ps_log2) - 1;
-        // page ids in warp-wide windows of 32 boxes, the next window loaded ahead
         const int bpt = box_rows >= 8 ? BN / box_rows : 1;  // boxes per tile (<= 16)
-        auto load_window = [&](int w) -> int {
-            const int key = (32 * w + lane) * box_rows;
-            return (box_rows >= 8 && key < L) ? prow[key >> ps_log2] : 0;
-        };
-        int w_cur = 0;
-        int pg_cur = load_window(0), pg_nxt = load_window(1);
-        // one K or V tile: wait for its slot, then TMA boxes (or gather)
-        auto load_tile = [&](int kv, int j, int pg_tile) -> bool {
-            const int ns = kv ? kVStages : kKStages;
-            const int s = j % ns;
-            const uint32_t ph = (j / ns) & 1;
-            const uint32_t full = BAR(kv ? B_VFULL(s) : B_KFULL(s));
-            const uint32_t empty = BAR(kv ? B_VEMPTY(s) : B_KEMPTY(s));
-            const uint32_t dst = (kv ? sV : sK) + s * Lo::KV_BYTES;
-            const int key0 = j * BN;
-            const int nkeys = min(BN, L - key0);  // keys of this tile that exist in pages
-            if (j >= ns && !mbar_wait_warp(empty, ph ^ 1, abort_flag, dev_status)) return false;
-            if (box_rows >= 8) {
-                const int nbox = (nkeys + box_rows - 1) / box_rows;  // <= 16
-                const bool bad = lane < nbox && (pg_tile < 0 || pg_tile >= num_pages);
-                const int nbad = __popc(__ballot_sync(0xffffffffu, bad));
-                if (lane == 0) {
-                    if (nbad) *bad_page = 1;
-                    mbar_arrive_expect_tx(
-                        full, static_cast<uint32_t>((nbox - nbad) * (D / 64) * box_rows * 128));
+        uint32_t kt = 0, vt = 0;  // K and V tiles loaded so far (ring position)
+        bool ok = true;
+        Item itm;
+        for (uint32_t ii = 0; ok; ++ii) {
+            // next item with work; invalid ones are flagged (and for bad
+            // lengths written as NaN) here and not published
+            int p = -1;
+            while (true) {
+                int q = 0;
+                if (lane == 0) q = static_cast<int>(atomicAdd(sched, 1u));
+                q = __shfl_sync(0xffffffffu, q, 0);
+                if (q >= n_items) break;
+                decode_item<G>(q, Hkv, B, mtiles, order, ranked, cu_seqlens, seq_lens, itm);
+                const int cu1 = itm.cu0 + itm.n;
+                if (itm.cu0 < 0 || itm.n < 0 || cu1 > Tq || (itm.r == 0 && itm.cu0 != 0) ||
+                    itm.n > max_q_len) {
+                    if (lane == 0 && dev_status) atomicOr(dev_status, PKV_DEV_BAD_CUSEQ);
+                    continue;
                 }
-                __syncwarp();
-                if (lane < nbox && !bad) {
-                    const int kk = key0 + lane * box_rows;
-                    const int row = (pg_tile << ps_log2) + (kk & ps_mask);
+                const int blk_tok0 = itm.mt * NQ * TOK;
+                if (blk_tok0 >= itm.n) continue;
+                if (itm.c < 0 || itm.L > cap) {
+                    if (lane == 0 && dev_status) atomicOr(dev_status, PKV_DEV_BAD_SEQLEN);
+                    const int blk_tok1 = min(itm.n, blk_tok0 + NQ * TOK);
+                    for (int idx = lane; idx < (blk_tok1 - blk_tok0) * G * D; idx += 32) {
+                        const int t = blk_tok0 + idx / (G * D);
+                        const int rem = idx % (G * D);
+                        out[((int64_t)(itm.cu0 + t) * Hq + (int64_t)itm.g * G) * D + rem] =
+                            __float2bfloat16_rn(__int_as_float(0x7fc00000));
+                    }
+                    continue;
+                }
+                p = q;
+                break;
+            }
+            // publish it (or the end) to the MMA and softmax warps
+            const int slot = ii % kItemSlots;
+            if (ii >= kItemSlots &&
+                !mbar_wait_warp(BAR(B_IEMPTY(slot)), ((ii / kItemSlots) & 1) ^ 1, abort_flag, dev_status))
+                break;
+            if (lane == 0) {
+                item_ring[slot] = p;
+                bad_flag[slot] = 0;
+                if (p >= 0) items[slot] = itm;
+                mbar_arrive(BAR(B_IFULL(slot)));
+            }
+            __syncwarp();
+            if (p < 0) break;
+
+            const int32_t *prow = page_table + (int64_t)itm.r * pt_stride;
+            const int L = itm.L, g = itm.g;
+            // page ids in warp-wide windows of 32 boxes, the next window loaded ahead
+            auto load_window = [&](int w) -> int {
+                const int key = (32 * w + lane) * box_rows;
+                return (box_rows >= 8 && key < L) ? prow[key >> ps_log2] : 0;
+            };
+            int w_cur = 0;
+            int pg_cur = load_window(0), pg_nxt = load_window(1);
+            // one K or V tile (tile j of the item, ring position t): wait for
+            // its slot, then TMA boxes (or gather)
+            auto load_tile = [&](int kv, int j, uint32_t t, int pg_tile) -> bool {
+                const int ns = kv ? kVStages : kKStages;
+                const int s = t % ns;
+                const uint32_t ph = (t / ns) & 1;
+                const uint32_t full = BAR(kv ? B_VFULL(s) : B_KFULL(s));
+                const uint32_t empty = BAR(kv ? B_VEMPTY(s) : B_KEMPTY(s));
+                const uint32_t dst = (kv ? sV : sK) + s * Lo::KV_BYTES;
+                const int key0 = j * BN;
+                const int nkeys = min(BN, L - key0);  // keys of this tile that exist in pages
+                if (t >= static_cast<uint32_t>(ns) && !mbar_wait_warp(empty, ph ^ 1, abort_flag, dev_status))
+                    return false;
+                if (box_rows >= 8) {
+                    const int nbox = (nkeys + box_rows - 1) / box_rows;  // <= 16
+                    const bool bad = lane < nbox && (pg_tile < 0 || pg_tile >= num_pages);
+                    const int nbad = __popc(__ballot_sync(0xffffffffu, bad));
+                    if (lane == 0) {
+                        if (nbad) bad_flag[slot] = 1;
+                        mbar_arrive_expect_tx(
+                            full, static_cast<uint32_t>((nbox - nbad) * (D / 64) * box_rows * 128));
+                    }
+                    __syncwarp();
+                    if (lane < nbox && !bad) {
+                        const int kk = key0 + lane * box_rows;
+                        const int row = (pg_tile << ps_log2) + (kk & ps_mask);
+#pragma unroll
+                        for (int blk = 0; blk < D / 64; ++blk)
+                            tma_load_3d(dst + blk * Lo::KBLK + lane * box_rows * 128, kv ? &vmap : &kmap,
+                                        full, blk * 64, g, row, pol_kv);
+                    }
+                } else {
+                    // small pages: gather 16-byte chunks, swizzle, zero rows past the sequence
+                    const __nv_bfloat16 *base = kv ? v_cache : k_cache;
+                    bool bad = false;
+                    for (int idx = lane; idx < BN * (D / 8); idx += 32) {
+                        const int key = idx / (D / 8), ch = idx % (D / 8);
+                        uint4 val = make_uint4(0u, 0u, 0u, 0u);
+                        if (key < nkeys) {
+                            const int kk = key0 + key;
+                            const int pg = prow[kk >> ps_log2];
+                            if (pg >= 0 && pg < num_pages) {
+                                const int64_t sl = ((int64_t)pg << ps_log2) + (kk & ps_mask);
+                                val = __ldg(reinterpret_cast<const uint4 *>(base + (sl * Hkv + g) * D +
+                                                                            ch * 8));
+                            } else {
+                                bad = true;
+                            }
+                        }
+                        *reinterpret_cast<uint4 *>(smem + (dst - smem_u32(smem)) +
+                                                   swz_offset(key, ch, BN)) = val;
+                    }
+                    if (__any_sync(0xffffffffu, bad) && lane == 0) bad_flag[slot] = 1;
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(full);
+                }
+                return true;
+            };
+            auto page_of_tile = [&](int j) -> int {
+                const int b0 = j * bpt;
+                if ((b0 >> 5) != w_cur) {
+                    w_cur = b0 >> 5;
+                    pg_cur = pg_nxt;
+                    pg_nxt = load_window(w_cur + 1);
+                }
+                return __shfl_sync(0xffffffffu, pg_cur, (b0 + (lane % bpt)) & 31);
+            };
+            // K(0) first: it needs only a free K slot; the Q tiles wait until
+            // the previous item's QK^T MMAs have read the Q buffer
+            int pg_prev = page_of_tile(0);
+            ok = load_tile(0, 0, kt, pg_prev);
+            if (ok && ii > 0)
+                ok = mbar_wait_warp(BAR(B_QEMPTY), (ii - 1) & 1, abort_flag, dev_status);
+            if (!ok) break;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(BAR(B_QFULL), static_cast<uint32_t>(NQ * Lo::Q_BYTES));
+#pragma unroll
+                for (int qt = 0; qt < NQ; ++qt)
 #pragma unroll
                     for (int blk = 0; blk < D / 64; ++blk)
-                        tma_load_3d(dst + blk * Lo::KBLK + lane * box_rows * 128, kv ? &vmap : &kmap,
-                                    full, blk * 64, g, row, pol_kv);
+                        tma_load_3d(sQ + qt * Lo::Q_BYTES + blk * Lo::BLK, &qmap, BAR(B_QFULL),
+                                    blk * 64, g * G, itm.cu0 + (qt ? itm.tbeg[1] : itm.tbeg[0]), pol_q);
+            }
+            __syncwarp();
+            // K runs one tile ahead of V: K(j+1) is needed right after PV(j)
+            for (int j = 0; ok && j < itm.n_kt; ++j) {
+                const int pg_j = pg_prev;
+                if (j + 1 < itm.n_kt) {
+                    pg_prev = page_of_tile(j + 1);
+                    ok = load_tile(0, j + 1, kt + j + 1, pg_prev);
                 }
-            } else {
-                // small pages: gather 16-byte chunks, swizzle, zero rows past the sequence
-                const __nv_bfloat16 *base = kv ? v_cache : k_cache;
-                bool bad = false;
-                for (int idx = lane; idx < BN * (D / 8); idx += 32) {
-                    const int key = idx / (D / 8), ch = idx % (D / 8);
-                    uint4 val = make_uint4(0u, 0u, 0u, 0u);
-                    if (key < nkeys) {
-                        const int kk = key0 + key;
-                        const int pg = prow[kk >> ps_log2];
-                        if (pg >= 0 && pg < num_pages) {
-                            const int64_t slot = ((int64_t)pg << ps_log2) + (kk & ps_mask);
-                            val = __ldg(reinterpret_cast<const uint4 *>(base + (slot * Hkv + g) * D +
-                                                                        ch * 8));
-                        } else {
-                            bad = true;
-                        }
-                    }
-                    *reinterpret_cast<uint4 *>(smem + (dst - smem_u32(smem)) +
-                                               swz_offset(key, ch, BN)) = val;
-                }
-                if (__any_sync(0xffffffffu, bad) && lane == 0) *bad_page = 1;
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(full);
+                ok = ok && load_tile(1, j, vt + j, pg_j);
             }
-            return true;
-        };
-        auto page_of_tile = [&](int j) -> int {
-            const int b0 = j * bpt;
-            if ((b0 >> 5) != w_cur) {
-                w_cur = b0 >> 5;
-                pg_cur = pg_nxt;
-                pg_nxt = load_window(w_cur + 1);
-            }
-            return __shfl_sync(0xffffffffu, pg_cur, (b0 + (lane % bpt)) & 31);
-        };
-        // K runs one tile ahead of V: K(j+1) is needed right after PV(j)
-        int pg_prev = page_of_tile(0);
-        bool ok = load_tile(0, 0, pg_prev);
-        for (int j = 0; ok && j < n_kt; ++j) {
-            const int pg_j = pg_prev;
-            if (j + 1 < n_kt) {
-                pg_prev = page_of_tile(j + 1);
-                ok = load_tile(0, j + 1, pg_prev);
-            }
-            ok = ok && load_tile(1, j, pg_j);
+            kt += itm.n_kt;
+            vt += itm.n_kt;
         }
     } else if (warp >= kMmaWarp) {
         // ================================================================ MMA issuers
         // Warp 9 + qt issues the MMAs of query tile qt, so one tile's issue never
-        // waits behind the other's.  Both warps step through every key tile to
-        // release the K and V slots (count NQ) in phase.
+        // waits behind the other's.  Both warps step through every key tile of
+        // every item to release the K and V slots (count NQ) in phase, and both
+        // take every item's Q (also when their tile has no rows).
         const int qt = warp - kMmaWarp;
         constexpr uint32_t idesc_s = instr_desc(BM, BN, false);
         constexpr uint32_t idesc_o = instr_desc(BM, D, true);
-        auto issue_s = [&](int j) {  // S(qt) = Q(qt) K(j)^T; K(j) is resident
-            const uint32_t kb = sK + (j % kKStages) * Lo::KV_BYTES;
+        auto issue_s = [&](uint32_t t) {  // S(qt) = Q(qt) K^T; K tile at ring position t
+            const uint32_t kb = sK + (t % kKStages) * Lo::KV_BYTES;
             const uint32_t qb = sQ + qt * Lo::Q_BYTES;
             tc_fence_after();
             if (lane == 0) {
@@ -347,65 +480,97 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             __syncwarp();
         };
-        auto issue_pv = [&](int j) {  // O(qt) += P(qt) V(j); P in TMEM, V in shared memory
-            const uint32_t vb = sV + (j % kVStages) * Lo::KV_BYTES;
+        auto issue_pv = [&](uint32_t t, bool acc) {  // O(qt) += P(qt) V; P in TMEM, V at ring position t
+            const uint32_t vb = sV + (t % kVStages) * Lo::KV_BYTES;
             tc_fence_after();
             if (lane == 0) {
 #pragma unroll
                 for (int kk = 0; kk < BN / 16; ++kk)
                     umma_bf16_ts(tm_o(qt), tm_s(qt) + kk * 8,
                                  smem_desc(vb + kk * 16 * 128, Lo::KBLK, 1024), idesc_o,
-                                 (j > 0 || kk > 0) ? 1u : 0u);
+                                 (acc || kk > 0) ? 1u : 0u);
                 umma_commit(BAR(B_ODONE(qt)));
             }
             __syncwarp();
         };
-        bool ok = mbar_wait_warp(BAR(B_QFULL), 0, abort_flag, dev_status) &&
-                  mbar_wait_warp(BAR(B_KFULL(0)), 0, abort_flag, dev_status);
-        if (ok) {
-            if (nkt[qt] > 0) issue_s(0);
-            if (lane == 0) umma_commit(BAR(B_KEMPTY(0)));
+        auto commit = [&](uint32_t bar) {
+            if (lane == 0) umma_commit(bar);
             __syncwarp();
-        }
-        for (int j = 0; ok && j < n_kt; ++j) {
-            const int s = j % kVStages;
-            if (!mbar_wait_warp(BAR(B_VFULL(s)), (j / kVStages) & 1, abort_flag, dev_status)) {
-                ok = false;
-                break;
-            }
-            if (j < nkt[qt]) {
-                if (j == n_kt - 1 && (j + 1) * BN > L) {
-                    // keys past the sequence end hold stale pool data (maybe NaN):
-                    // zero those V rows so that P = 0 there contributes exactly 0
-                    // (both MMA warps write the same zeros before their own PV)
-                    const uint32_t vb = sV + s * Lo::KV_BYTES;
-                    const int first = L - j * BN;
-                    for (int idx = lane; idx < (BN - first) * (D / 8); idx += 32) {
-                        const int key = first + idx / (D / 8), ch = idx % (D / 8);
-                        *reinterpret_cast<uint4 *>(smem + (vb - smem_u32(smem)) +
-                                                   swz_offset(key, ch, BN)) = make_uint4(0u, 0u, 0u, 0u);
+        };
+        uint32_t kt = 0, vt = 0;  // ring positions of the current item's K(0) and V(0)
+        uint32_t pc = 0;          // P tiles consumed by this warp (all items)
+        uint32_t wk = 0;          // items in which this tile had rows
+        bool ok = true;
+        for (uint32_t ii = 0; ok; ++ii) {
+            const int slot = ii % kItemSlots;
+            if (!mbar_wait_warp(BAR(B_IFULL(slot)), (ii / kItemSlots) & 1, abort_flag, dev_status)) break;
+            const int p = item_ring[slot];
+            if (p < 0) break;
+            const Item &itm = items[slot];
+            const int my_kt = qt ? itm.nkt[1] : itm.nkt[0], n_kt = itm.n_kt, L = itm.L;
+            ok = mbar_wait_warp(BAR(B_QFULL), ii & 1, abort_flag, dev_status) &&
+                 mbar_wait_warp(BAR(B_KFULL(kt % kKStages)), (kt / kKStages) & 1, abort_flag, dev_status);
+            if (!ok) break;
+            if (my_kt > 0) issue_s(kt);
+            if (my_kt <= 1) commit(BAR(B_QEMPTY));  // this warp's QK^T MMAs of the item are issued
+            commit(BAR(B_KEMPTY(kt % kKStages)));
+            for (int j = 0; j < n_kt; ++j) {
+                const uint32_t tv = vt + j;
+                const int s = tv % kVStages;
+                if (!mbar_wait_warp(BAR(B_VFULL(s)), (tv / kVStages) & 1, abort_flag, dev_status)) {
+                    ok = false;
+                    break;
+                }
+                if (j < my_kt) {
+                    if (j == n_kt - 1 && (j + 1) * BN > L) {
+                        // keys past the sequence end hold stale pool data (maybe NaN):
+                        // zero those V rows so that P = 0 there contributes exactly 0
+                        // (both MMA warps write the same zeros before their own PV)
+                        const uint32_t vb = sV + s * Lo::KV_BYTES;
+                        const int first = L - j * BN;
+                        for (int idx = lane; idx < (BN - first) * (D / 8); idx += 32) {
+                            const int key = first + idx / (D / 8), ch = idx % (D / 8);
+                            *reinterpret_cast<uint4 *>(smem + (vb - smem_u32(smem)) +
+                                                       swz_offset(key, ch, BN)) = make_uint4(0u, 0u, 0u, 0u);
+                        }
+                        fence_proxy_async_smem();
+                        __syncwarp();
                     }
-                    fence_proxy_async_smem();
-                    __syncwarp();
+                    if (!mbar_wait_warp(BAR(B_PFULL(qt)), pc & 1, abort_flag, dev_status)) {
+                        ok = false;
+                        break;
+                    }
+                    ++pc;
+                    // the first PV of an item overwrites O: the previous item's
+                    // output must have been read out of tensor memory
+                    if (j == 0 && wk > 0 &&
+                        !mbar_wait_warp(BAR(B_OFREE(qt)), (wk - 1) & 1, abort_flag, dev_status)) {
+                        ok = false;
+                        break;
+                    }
+                    issue_pv(tv, j > 0);
                 }
-                if (!mbar_wait_warp(BAR(B_PFULL(qt)), j & 1, abort_flag, dev_status)) {
-                    ok = false;
-                    break;
+                commit(BAR(B_VEMPTY(s)));
+                if (j + 1 < n_kt) {
+                    const uint32_t tk = kt + j + 1;
+                    if (!mbar_wait_warp(BAR(B_KFULL(tk % kKStages)), (tk / kKStages) & 1, abort_flag,
+                                        dev_status)) {
+                        ok = false;
+                        break;
+                    }
+                    if (j + 1 < my_kt) {
+                        issue_s(tk);
+                        if (j + 1 == my_kt - 1) commit(BAR(B_QEMPTY));
+                    }
+                    commit(BAR(B_KEMPTY(tk % kKStages)));
                 }
-                issue_pv(j);
             }
-            if (lane == 0) umma_commit(BAR(B_VEMPTY(s)));
-            __syncwarp();
-            if (j + 1 < n_kt) {
-                const int s1 = (j + 1) % kKStages;
-                if (!mbar_wait_warp(BAR(B_KFULL(s1)), ((j + 1) / kKStages) & 1, abort_flag,
-                                    dev_status)) {
-                    ok = false;
-                    break;
-                }
-                if (j + 1 < nkt[qt]) issue_s(j + 1);
-                if (lane == 0) umma_commit(BAR(B_KEMPTY(s1)));
+            kt += n_kt;
+            vt += n_kt;
+            if (my_kt > 0) ++wk;
+            if (ok) {
                 __syncwarp();
+                if (lane == 0) mbar_arrive(BAR(B_IEMPTY(slot)));
             }
         }
     } else {
@@ -413,138 +578,197 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int qt = warp >> 2;                  // query tile of this warpgroup
         const int row = tid & 127;                 // TMEM lane == tile row
         const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-        const int tok = tbeg[qt] + row / G;
-        const bool row_valid = tok < tend[qt];
-        const int lim = c + tok;                   // last key this row may see
-        const int my_kt = nkt[qt];
-        float m_ref = kNegBig, l_sum = 0.f;
+        uint32_t sc = 0;                  // S tiles consumed by this warpgroup (all items)
+        uint32_t steps_a = 0, steps_b = 0;  // key-tile steps completed by each warpgroup
         bool ok = true;
-        // tcgen05.ld/st are warp-collective: every wait outcome is warp-uniform
-        for (int j = 0; j < my_kt; ++j) {
-            // S(j) complete implies PV(j-1) complete: O is stable and P free
-            ok = mbar_wait_warp(BAR(B_SFULL(qt)), j & 1, abort_flag, dev_status);
-            if (!ok) break;
-            // The two softmax warpgroups take turns (A(0), B(0), A(1), B(1), ...)
-            // so that one's exponentials always overlap the other's MMAs instead
-            // of both competing for the same SM sub-partitions at once.
-            if (qt == 0 ? (j >= 1 && j - 1 < nkt[1]) : (j < nkt[0])) {
-                const int other = 1 - qt;
-                const int done = qt == 0 ? j - 1 : j;  // key tile the other group must have finished
-                ok = mbar_wait_warp(BAR(B_TURN(other)), done & 1, abort_flag, dev_status);
+        for (uint32_t ii = 0; ok; ++ii) {
+            const int slot = ii % kItemSlots;
+            if (!mbar_wait_warp(BAR(B_IFULL(slot)), (ii / kItemSlots) & 1, abort_flag, dev_status)) break;
+            const int p = item_ring[slot];
+            if (p < 0) break;
+            const Item &itm = items[slot];
+            const int tok = (qt ? itm.tbeg[1] : itm.tbeg[0]) + row / G;
+            const bool row_valid = tok < (qt ? itm.tend[1] : itm.tend[0]);
+            const bool warp_live = __any_sync(0xffffffffu, row_valid);
+            const int lim = itm.c + tok;  // last key this row may see
+            const int my_kt = (qt ? itm.nkt[1] : itm.nkt[0]);
+            float m_ref = kNegBig, l_sum = 0.f;
+            // tcgen05.ld/st are warp-collective: every wait outcome is warp-uniform
+            for (int j = 0; j < my_kt; ++j) {
+                // S(j) complete implies PV(j-1) complete: O is stable and P free
+                ok = mbar_wait_warp(BAR(B_SFULL(qt)), (sc + j) & 1, abort_flag, dev_status);
                 if (!ok) break;
-            }
-            tc_fence_after();
-            // all 128 scores of this row in registers (one wait for four loads)
-            uint32_t sv[BN];
-#pragma unroll
-            for (int cc = 0; cc < BN / 32; ++cc) tmem_ld_32cols(tm_s(qt) + lane_off + cc * 32, sv + cc * 32);
-            tmem_wait_ld();
-            // causal mask by selection (-inf), only on tiles that cross some
-            // row's limit (a warp-uniform branch)
-            const int key0 = j * BN;
-            if (__any_sync(0xffffffffu, !row_valid || key0 + BN - 1 > lim)) {
-                const int nvalid = row_valid ? lim - key0 + 1 : 0;  // keys kept in this row
-#pragma unroll
-                for (int i = 0; i < BN; ++i)
-                    if (i >= nvalid) sv[i] = __float_as_uint(-INFINITY);
-            }
-            float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-            for (int i = 0; i < BN; i += 2)
-                mx4[(i >> 1) & 3] = fmax3(mx4[(i >> 1) & 3], __uint_as_float(sv[i]), __uint_as_float(sv[i + 1]));
-            const float mt_max = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * scale_log2;
-            const bool need = (j == 0) ? false : (mt_max > m_ref + kRescaleLog2);
-            const bool warp_need = __any_sync(0xffffffffu, need);
-            float alpha = 1.f;
-            if (j == 0) {
-                m_ref = fmaxf(mt_max, kNegBig);  // stays finite for rows with no key
-            } else if (warp_need) {
-                const float mn = fmaxf(m_ref, mt_max);
-                alpha = ex2(m_ref - mn);
-                m_ref = mn;
-            }
-            // p = 2^(s*scale*log2e - m_ref) on the SFU, packed to bf16 pairs and
-            // written 32 keys at a time into tensor memory over the S columns
-            // already read (keys 32cc.. -> columns 16cc..)
-            const float neg_m = -m_ref;
-            float rs[4] = {0.f, 0.f, 0.f, 0.f};  // two packed pairs of partial sums
-#pragma unroll
-            for (int cc = 0; cc < BN / 32; ++cc) {
-                uint32_t pk[16];
-#pragma unroll
-                for (int q = 0; q < 16; ++q) {
-                    const int i = cc * 32 + 2 * q;
-                    float x0, x1;
-                    fma2(x0, x1, __uint_as_float(sv[i]), __uint_as_float(sv[i + 1]), scale_log2,
-                         scale_log2, neg_m, neg_m);
-                    const float p0 = ex2(x0), p1 = ex2(x1);
-                    add2(rs[2 * (q & 1)], rs[2 * (q & 1) + 1], p0, p1);
-                    pk[q] = pack_bf16x2(p0, p1);
+                // The two softmax warpgroups take turns (A(0), B(0), A(1), B(1), ...,
+                // then B's extra step, then the next item) so that one's
+                // exponentials overlap the other's MMAs instead of both competing
+                // for the same SM sub-partitions at once: a step waits until the
+                // other group has finished the steps before it in that order.
+                {
+                    const uint32_t need = qt == 0 ? (j == 0 ? steps_b : steps_b + min(j, itm.nkt[1]))
+                                                  : steps_a + min(j + 1, itm.nkt[0]);
+                    ok = wait_count(turn_cnt + (1 - qt), static_cast<int>(4 * need), abort_flag, dev_status);
+                    if (!ok) break;
                 }
-                tmem_st_16cols(tm_s(qt) + lane_off + cc * 16, pk);
-            }
-            l_sum = l_sum * alpha + ((rs[0] + rs[1]) + (rs[2] + rs[3]));
-            // rescale the output row to the new reference (PV(j-1) is complete)
-            if (warp_need) {
+                if (warp_live) {
+                    tc_fence_after();
+                    // all 128 scores of this row in registers (one wait for four loads)
+                    uint32_t sv[BN];
 #pragma unroll
-                for (int cc = 0; cc < D / 32; ++cc) {
-                    uint32_t ov[32];
-                    tmem_ld_32cols(tm_o(qt) + lane_off + cc * 32, ov);
+                    for (int cc = 0; cc < BN / 32; ++cc)
+                        tmem_ld_32cols(tm_s(qt) + lane_off + cc * 32, sv + cc * 32);
                     tmem_wait_ld();
+                    // causal mask by selection (-inf), only on tiles that cross some
+                    // row's limit (a warp-uniform branch)
+                    const int key0 = j * BN;
+                    if (__any_sync(0xffffffffu, !row_valid || key0 + BN - 1 > lim)) {
+                        const int nvalid = row_valid ? lim - key0 + 1 : 0;  // keys kept in this row
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-                    tmem_st_32cols(tm_o(qt) + lane_off + cc * 32, ov);
+                        for (int i = 0; i < BN; ++i)
+                            if (i >= nvalid) sv[i] = __float_as_uint(-INFINITY);
+                    }
+                    float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+                    for (int i = 0; i < BN; i += 2)
+                        mx4[(i >> 1) & 3] =
+                            fmax3(mx4[(i >> 1) & 3], __uint_as_float(sv[i]), __uint_as_float(sv[i + 1]));
+                    const float mt_max = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * scale_log2;
+                    const bool need = (j == 0) ? false : (mt_max > m_ref + kRescaleLog2);
+                    const bool warp_need = __any_sync(0xffffffffu, need);
+                    float alpha = 1.f;
+                    if (j == 0) {
+                        m_ref = fmaxf(mt_max, kNegBig);  // stays finite for rows with no key
+                    } else if (warp_need) {
+                        const float mn = fmaxf(m_ref, mt_max);
+                        alpha = ex2(m_ref - mn);
+                        m_ref = mn;
+                    }
+                    // p = 2^(s*scale*log2e - m_ref) on the SFU, packed to bf16 pairs and
+                    // written 32 keys at a time into tensor memory over the S columns
+                    // already read (keys 32cc.. -> columns 16cc..)
+                    const float neg_m = -m_ref;
+                    float rs[4] = {0.f, 0.f, 0.f, 0.f};  // two packed pairs of partial sums
+#pragma unroll
+                    for (int cc = 0; cc < BN / 32; ++cc) {
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int q = 0; q < 16; ++q) {
+                            const int i = cc * 32 + 2 * q;
+                            float x0, x1;
+                            fma2(x0, x1, __uint_as_float(sv[i]), __uint_as_float(sv[i + 1]), scale_log2,
+                                 scale_log2, neg_m, neg_m);
+                            const float p0 = ex2(x0), p1 = ex2(x1);
+                            add2(rs[2 * (q & 1)], rs[2 * (q & 1) + 1], p0, p1);
+                            pk[q] = pack_bf16x2(p0, p1);
+                        }
+                        tmem_st_16cols(tm_s(qt) + lane_off + cc * 16, pk);
+                    }
+                    l_sum = l_sum * alpha + ((rs[0] + rs[1]) + (rs[2] + rs[3]));
+                    // rescale the output row to the new reference (PV(j-1) is complete)
+                    if (warp_need) {
+#pragma unroll
+                        for (int cc = 0; cc < D / 32; ++cc) {
+                            uint32_t ov[32];
+                            tmem_ld_32cols(tm_o(qt) + lane_off + cc * 32, ov);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int e = 0; e < 32; ++e)
+                                ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+                            tmem_st_32cols(tm_o(qt) + lane_off + cc * 32, ov);
+                        }
+                    }
+                    tmem_wait_st();  // P and O stores
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(BAR(B_PFULL(qt)));
+                    atomicAdd(turn_cnt + qt, 1);
                 }
             }
-            tmem_wait_st();  // P and O stores
-            tc_fence_before();
+            if (!ok) break;
+            if (my_kt > 0) {
+                ok = mbar_wait_warp(BAR(B_ODONE(qt)), (sc + my_kt - 1) & 1, abort_flag, dev_status);
+                if (!ok) break;
+                tc_fence_after();
+                // the output row out of tensor memory 32 columns at a time,
+                // normalised, packed to bf16 and stored; then O is free for the
+                // next item's first PV
+                const bool poison = (bad_flag[slot] != 0) || (*abort_flag != 0);
+                const float inv = row_valid ? 1.f / l_sum : 0.f;
+                __nv_bfloat16 *orow =
+                    out + ((int64_t)(itm.cu0 + tok) * Hq + (int64_t)itm.g * G + row % G) * D;
+                if (warp_live) {
+#pragma unroll
+                    for (int cc = 0; cc < D / 32; ++cc) {
+                        uint32_t ov[32];
+                        tmem_ld_32cols(tm_o(qt) + lane_off + cc * 32, ov);
+                        tmem_wait_ld();
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int e = 0; e < 32; e += 2)
+                            pk[e / 2] = poison ? 0x7fc07fc0u  // two bf16 NaNs
+                                               : pack_bf16x2(__uint_as_float(ov[e]) * inv,
+                                                             __uint_as_float(ov[e + 1]) * inv);
+                        if (row_valid) {
+#pragma unroll
+                            for (int q4 = 0; q4 < 4; ++q4)
+                                reinterpret_cast<uint4 *>(orow + cc * 32)[q4] =
+                                    make_uint4(pk[q4 * 4], pk[q4 * 4 + 1], pk[q4 * 4 + 2], pk[q4 * 4 + 3]);
+                        }
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(BAR(B_OFREE(qt)));
+                if (poison && tid == 0 && dev_status && bad_flag[slot])
+                    atomicOr(dev_status, PKV_DEV_BAD_PAGE);
+            }
+            sc += my_kt;
+            steps_a += itm.nkt[0];
+            steps_b += itm.nkt[1];
             __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(BAR(B_PFULL(qt)));
-                mbar_arrive(BAR(B_TURN(qt)));
-            }
+            if (lane == 0) mbar_arrive(BAR(B_IEMPTY(slot)));
         }
-        if (ok && my_kt > 0) ok = mbar_wait_warp(BAR(B_ODONE(qt)), (my_kt - 1) & 1, abort_flag, dev_status);
-        tc_fence_after();
-        __syncthreads();
-        const bool poison = (*bad_page != 0) || (*abort_flag != 0) || !ok;
-        if (my_kt > 0) {
-            // every lane takes part in the warp-wide TMEM loads; only valid rows store
-            const float inv = row_valid ? 1.f / l_sum : 0.f;
-            __nv_bfloat16 *orow = out + ((int64_t)(cu0 + tok) * Hq + (int64_t)g * G + row % G) * D;
-#pragma unroll
-            for (int cc = 0; cc < D / 32; ++cc) {
-                uint32_t ov[32];
-                tmem_ld_32cols(tm_o(qt) + lane_off + cc * 32, ov);
-                tmem_wait_ld();
-                uint32_t pk[16];
-#pragma unroll
-                for (int e = 0; e < 32; e += 2) {
-                    float a = __uint_as_float(ov[e]) * inv, bb = __uint_as_float(ov[e + 1]) * inv;
-                    if (poison) a = bb = __int_as_float(0x7fc00000);
-                    pk[e / 2] = pack_bf16x2(a, bb);
-                }
-                if (row_valid) {
-#pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4)
-                        reinterpret_cast<uint4 *>(orow + cc * 32)[q4] =
-                            make_uint4(pk[q4 * 4], pk[q4 * 4 + 1], pk[q4 * 4 + 2], pk[q4 * 4 + 3]);
-                }
-            }
-        }
-        if (poison && tid == 0 && dev_status && *bad_page) atomicOr(dev_status, PKV_DEV_BAD_PAGE);
-        tc_fence_before();
-        __syncthreads();
-        return;
     }
-    // producer and MMA warps meet the softmax warps here, then free TMEM
-    __syncthreads();
+    // all roles meet here, then the TMEM is freed and the queue counters of
+    // this call are reset by the last block to finish
     tc_fence_before();
     __syncthreads();
     if (warp == kMmaWarp) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
+    if (tid == 0) {
+        __threadfence();
+        if (atomicAdd(sched + 1, 1u) == gridDim.x - 1) {
+            sched[0] = 0;
+            sched[1] = 0;
+            __threadfence();
+        }
+    }
+}
+
+// Queue counters for this call: a slot of g_sched on the current device, taken
+// round-robin, so calls in flight at the same time (up to kSchedSlots of
+// them) use different counters.  The device address of g_sched is looked up
+// once per device.
+static unsigned int *sched_counters() {
+    static std::mutex mu;
+    static unsigned int *base[64] = {};
+    static std::atomic<unsigned int> next{0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    unsigned int *b = nullptr;
+    {
+        std::lock_guard<std::mutex> lk(mu);
+        if (!base[dev]) {
+            void *p = nullptr;
+            if (cudaGetSymbolAddress(&p, g_sched) != cudaSuccess || !p) return nullptr;
+            base[dev] = static_cast<unsigned int *>(p);
+        }
+        b = base[dev];
+    }
+    return b + 2 * (next.fetch_add(1u) % kSchedSlots);
 }
 
 template <int D, int G>
@@ -588,13 +812,17 @@ static pkv_status launch(const pkv_bf16 *q, const int32_t *cu, const pkv_bf16 *k
     int ps_log2 = 0;
     while ((1 << ps_log2) < page_size) ++ps_log2;
     const int mtiles = (max_q_len + NQ * TOK - 1) / (NQ * TOK);
-    const int64_t grid = static_cast<int64_t>(mtiles) * B * Hkv;
-    if (grid == 0) return PKV_OK;
-    if (grid > 0x7fffffffll) return PKV_EUNSUPPORTED;
+    const int64_t items = static_cast<int64_t>(mtiles) * B * Hkv;
+    if (items == 0) return PKV_OK;
+    if (items > 0x7fffffffll) return PKV_EUNSUPPORTED;
+    unsigned int *sched = sched_counters();
+    if (!sched) return PKV_ECUDA;
+    // persistent: one block per SM (fewer when there are fewer items)
+    const int grid = items < dev.sm_count ? static_cast<int>(items) : dev.sm_count;
     prefill_kernel<D, G><<<static_cast<unsigned>(grid), kThreads, Layout<D>::bytes(), stream>>>(
         qmap, kmap, vmap, reinterpret_cast<const __nv_bfloat16 *>(k_cache),
         reinterpret_cast<const __nv_bfloat16 *>(v_cache), cu, page_table, pt_stride, seq_lens, B, Tq,
-        max_q_len, Hkv, ps_log2, box_rows, num_pages, scale * kLog2e, mtiles, dev_status,
+        max_q_len, Hkv, ps_log2, box_rows, num_pages, scale * kLog2e, mtiles, sched, dev_status,
         reinterpret_cast<__nv_bfloat16 *>(out));
     return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ECUDA;
 }
