@@ -65,7 +65,7 @@ constexpr int kKStages = 2, kVStages = 2;
 constexpr int kProducerWarp = 8, kMmaWarp = 9;  // warps 9 and 10 issue the MMAs of tiles A and B
 constexpr int kItemSlots = 2;                   // items published ahead of the consumers
 constexpr int kItemConsumers = 2 + 8;           // MMA warps + softmax warps
-constexpr int kRankGroups = kThreads;           // up to this many (token block, request) groups
+constexpr int kRankGroups = 256;                // up to this many (token block, request) groups
                                                 // are ranked by work in the kernel
 constexpr int kSchedSlots = 256;                // queue counters for calls in flight at once
 constexpr float kLog2e = 1.4426950408889634f;
@@ -86,7 +86,8 @@ struct Layout {
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_K = OFF_Q + NQ * Q_BYTES;
     static constexpr int OFF_V = OFF_K + kKStages * KV_BYTES;
-    static constexpr int OFF_BAR = OFF_V + kVStages * KV_BYTES;
+    static constexpr int OFF_STAGE = OFF_V + kVStages * KV_BYTES;  // output staging, 2 KB per softmax warp
+    static constexpr int OFF_BAR = OFF_STAGE + 8 * 2048;
     // qfull, qempty, kfull/kempty[kKStages], vfull/vempty[kVStages],
     // per query tile: sfull, pfull, odone, ofree; item full/empty[kItemSlots]
     static constexpr int NBARS = 2 + 2 * kKStages + 2 * kVStages + NQ * 4 + 2 * kItemSlots;
@@ -427,22 +428,48 @@ __global__ void __launch_bounds__(kThreads, 1)
                 return __shfl_sync(0xffffffffu, pg_cur, (b0 + (lane % bpt)) & 31);
             };
             // K(0) first: it needs only a free K slot; the Q tiles wait until
-            // the previous item's QK^T MMAs have read the Q buffer
+            // the previous item's QK^T MMAs have read the Q buffer.  Until then
+            // the Q tiles and the first K and V tiles are prefetched into L2.
+            // (The first item's Q tiles have nothing to wait for: they are
+            // loaded at once, before the page ids are read.)
+            auto load_q = [&]() {
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(BAR(B_QFULL), static_cast<uint32_t>(NQ * Lo::Q_BYTES));
+#pragma unroll
+                    for (int qt = 0; qt < NQ; ++qt)
+#pragma unroll
+                        for (int blk = 0; blk < D / 64; ++blk)
+                            tma_load_3d(sQ + qt * Lo::Q_BYTES + blk * Lo::BLK, &qmap, BAR(B_QFULL),
+                                        blk * 64, g * G, itm.cu0 + (qt ? itm.tbeg[1] : itm.tbeg[0]), pol_q);
+                }
+                __syncwarp();
+            };
+            if (ii == 0) load_q();
             int pg_prev = page_of_tile(0);
-            ok = load_tile(0, 0, kt, pg_prev);
-            if (ok && ii > 0)
-                ok = mbar_wait_warp(BAR(B_QEMPTY), (ii - 1) & 1, abort_flag, dev_status);
-            if (!ok) break;
-            if (lane == 0) {
-                mbar_arrive_expect_tx(BAR(B_QFULL), static_cast<uint32_t>(NQ * Lo::Q_BYTES));
+            if (ii > 0 && lane == 0) {
 #pragma unroll
                 for (int qt = 0; qt < NQ; ++qt)
 #pragma unroll
                     for (int blk = 0; blk < D / 64; ++blk)
-                        tma_load_3d(sQ + qt * Lo::Q_BYTES + blk * Lo::BLK, &qmap, BAR(B_QFULL),
-                                    blk * 64, g * G, itm.cu0 + (qt ? itm.tbeg[1] : itm.tbeg[0]), pol_q);
+                        tma_prefetch_3d(&qmap, blk * 64, g * G, itm.cu0 + itm.tbeg[qt]);
             }
-            __syncwarp();
+            if (box_rows >= 8) {
+                const int nbox0 = (min(BN, L) + box_rows - 1) / box_rows;
+                if (lane < nbox0 && pg_prev >= 0 && pg_prev < num_pages) {
+                    const int row = pg_prev << ps_log2;  // tile 0 starts at key 0: box offset (lane * box_rows) & ps_mask
+#pragma unroll
+                    for (int blk = 0; blk < D / 64; ++blk) {
+                        tma_prefetch_3d(&kmap, blk * 64, g, row + ((lane * box_rows) & ps_mask));
+                        tma_prefetch_3d(&vmap, blk * 64, g, row + ((lane * box_rows) & ps_mask));
+                    }
+                }
+            }
+            ok = load_tile(0, 0, kt, pg_prev);
+            if (ok && ii > 0) {
+                ok = mbar_wait_warp(BAR(B_QEMPTY), (ii - 1) & 1, abort_flag, dev_status);
+                if (ok) load_q();
+            }
+            if (!ok) break;
             // K runs one tile ahead of V: K(j+1) is needed right after PV(j)
             for (int j = 0; ok && j < itm.n_kt; ++j) {
                 const int pg_j = pg_prev;
@@ -691,12 +718,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!ok) break;
                 tc_fence_after();
                 // the output row out of tensor memory 32 columns at a time,
-                // normalised, packed to bf16 and stored; then O is free for the
-                // next item's first PV
+                // normalised and packed to bf16; each warp passes its 32 rows'
+                // 64-byte pieces through shared memory so that the stores to
+                // global memory are whole 64-byte runs (8 rows per instruction)
+                // instead of 16 bytes from each of 32 rows
                 const bool poison = (bad_flag[slot] != 0) || (*abort_flag != 0);
                 const float inv = row_valid ? 1.f / l_sum : 0.f;
-                __nv_bfloat16 *orow =
-                    out + ((int64_t)(itm.cu0 + tok) * Hq + (int64_t)itm.g * G + row % G) * D;
+                const uint32_t stage = smem_u32(smem + Lo::OFF_STAGE) + warp * 2048;
+                const int tbeg_q = qt ? itm.tbeg[1] : itm.tbeg[0];
+                const int tend_q = qt ? itm.tend[1] : itm.tend[0];
+                const int64_t out_row0 = (int64_t)itm.cu0 * Hq + (int64_t)itm.g * G;
                 if (warp_live) {
 #pragma unroll
                     for (int cc = 0; cc < D / 32; ++cc) {
@@ -709,12 +740,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                             pk[e / 2] = poison ? 0x7fc07fc0u  // two bf16 NaNs
                                                : pack_bf16x2(__uint_as_float(ov[e]) * inv,
                                                              __uint_as_float(ov[e + 1]) * inv);
-                        if (row_valid) {
+                        // row `lane`, 16-byte piece q at (q ^ (lane / 2 % 4)): conflict-free
 #pragma unroll
-                            for (int q4 = 0; q4 < 4; ++q4)
-                                reinterpret_cast<uint4 *>(orow + cc * 32)[q4] =
-                                    make_uint4(pk[q4 * 4], pk[q4 * 4 + 1], pk[q4 * 4 + 2], pk[q4 * 4 + 3]);
+                        for (int q = 0; q < 4; ++q)
+                            sts128(stage + lane * 64 + ((q ^ ((lane >> 1) & 3)) << 4),
+                                   make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]));
+                        __syncwarp();
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const int rl = 8 * k + (lane >> 2), q = lane & 3;
+                            const uint4 v = lds128(stage + rl * 64 + ((q ^ ((rl >> 1) & 3)) << 4));
+                            const int rt = (warp & 3) * 32 + rl;  // tile row
+                            const int t = tbeg_q + rt / G;
+                            if (t < tend_q)
+                                reinterpret_cast<uint4 *>(
+                                    out + (out_row0 + (int64_t)t * Hq + rt % G) * D + cc * 32)[q] = v;
                         }
+                        __syncwarp();
                     }
                 }
                 tc_fence_before();
