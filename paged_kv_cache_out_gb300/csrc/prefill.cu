@@ -194,7 +194,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int *item_ring = misc + 1;  // [kItemSlots]: published item, -1 = no more
     volatile int *bad_flag = misc + 3;   // [kItemSlots]: a page id of that item was invalid
     volatile int *n_items_s = misc + 5;
-    int *turn_cnt = const_cast<int *>(misc + 6);  // [NQ]: key-tile steps finished x 4 warps
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Lo::OFF_MISC + 32);
     int *order = reinterpret_cast<int *>(smem + Lo::OFF_RANK);
     Item *items = reinterpret_cast<Item *>(smem + Lo::OFF_ITEMS);  // the published items, decoded
@@ -243,8 +242,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         *abort_flag = 0;
         *n_items_s = 0;
-        turn_cnt[0] = 0;
-        turn_cnt[1] = 0;
         fence_mbar_init();
     }
     if (warp == kMmaWarp) {
@@ -606,7 +603,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int row = tid & 127;                 // TMEM lane == tile row
         const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
         uint32_t sc = 0;                  // S tiles consumed by this warpgroup (all items)
-        uint32_t steps_a = 0, steps_b = 0;  // key-tile steps completed by each warpgroup
         bool ok = true;
         for (uint32_t ii = 0; ok; ++ii) {
             const int slot = ii % kItemSlots;
@@ -625,17 +621,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // S(j) complete implies PV(j-1) complete: O is stable and P free
                 ok = mbar_wait_warp(BAR(B_SFULL(qt)), (sc + j) & 1, abort_flag, dev_status);
                 if (!ok) break;
-                // The two softmax warpgroups take turns (A(0), B(0), A(1), B(1), ...,
-                // then B's extra step, then the next item) so that one's
-                // exponentials overlap the other's MMAs instead of both competing
-                // for the same SM sub-partitions at once: a step waits until the
-                // other group has finished the steps before it in that order.
-                {
-                    const uint32_t need = qt == 0 ? (j == 0 ? steps_b : steps_b + min(j, itm.nkt[1]))
-                                                  : steps_a + min(j + 1, itm.nkt[0]);
-                    ok = wait_count(turn_cnt + (1 - qt), static_cast<int>(4 * need), abort_flag, dev_status);
-                    if (!ok) break;
-                }
                 if (warp_live) {
                     tc_fence_after();
                     // all 128 scores of this row in registers (one wait for four loads)
@@ -707,10 +692,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(BAR(B_PFULL(qt)));
-                    atomicAdd(turn_cnt + qt, 1);
-                }
+                if (lane == 0) mbar_arrive(BAR(B_PFULL(qt)));
             }
             if (!ok) break;
             if (my_kt > 0) {
@@ -766,8 +748,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     atomicOr(dev_status, PKV_DEV_BAD_PAGE);
             }
             sc += my_kt;
-            steps_a += itm.nkt[0];
-            steps_b += itm.nkt[1];
             __syncwarp();
             if (lane == 0) mbar_arrive(BAR(B_IEMPTY(slot)));
         }
