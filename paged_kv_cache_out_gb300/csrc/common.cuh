@@ -81,31 +81,6 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     }
 }
 
-// Wait until the shared-memory counter *cnt reaches target (a scheduling wait
-// between warps of one block, polled with short sleeps).  Gives up like
-// mbar_wait.  Warp-uniform outcome.
-__device__ __forceinline__ bool wait_count(const int *cnt, int target, volatile int *abort,
-                                           int32_t *dev_status) {
-    const volatile int *c = cnt;
-    bool ok = true;
-    if (*c < target) {
-        const uint64_t t0 = global_timer_ns();
-        for (uint32_t i = 1; *c < target; ++i) {
-            __nanosleep(32);
-            if ((i & 15) == 0) {
-                if (*abort) { ok = false; break; }
-                if (global_timer_ns() - t0 > kWaitLimitNs) {
-                    *abort = 1;
-                    if (dev_status) atomicOr(dev_status, PKV_DEV_TIMEOUT);
-                    ok = false;
-                    break;
-                }
-            }
-        }
-    }
-    return __all_sync(0xffffffffu, ok);
-}
-
 // The same wait taken by all 32 lanes of a warp, with one outcome for all of
 // them, so that warp-collective instructions after it are never divergent.
 __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int *abort,
@@ -192,23 +167,6 @@ __device__ __forceinline__ float ex2(float x) {  // 2^x on the SFU
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
-}
-
-// 2^x on the FMA pipe, for x in [-125, 126]: x = j + f with j = round(x) (the
-// 1.5 * 2^23 addition leaves round(x) in the low mantissa bits) and
-// f in [-1/2, 1/2]; 2^f by a cubic fitted here to 2^f on [-1/2, 1/2]
-// (Chebyshev-node least squares, reweighted towards minimax relative error:
-// max relative error 7.5e-5 in fp32); 2^j is added to the exponent field.
-// Used for part of the softmax exponentials so the SFU is not the only unit
-// computing them.
-__device__ __forceinline__ float exp2_poly(float x) {
-    const float t = x + 12582912.0f;
-    const int j = __float_as_int(t) - 0x4B400000;
-    const float f = x - (t - 12582912.0f);
-    float p = fmaf(0.0551716648042202f, f, 0.2426111251115799f);
-    p = fmaf(p, f, 0.6932609677314758f);
-    p = fmaf(p, f, 0.9999280571937561f);
-    return __int_as_float(__float_as_int(p) + (j << 23));
 }
 
 // max of three floats in one instruction
