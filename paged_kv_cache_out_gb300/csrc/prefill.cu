@@ -45,8 +45,8 @@
 //               item reads O out of tensor memory (then frees it for the next
 //               item), normalises and stores the row.  A warp whose 32 rows
 //               are all past the request's last token does no arithmetic.
-// While one tile's softmax runs, the tensor core works on the other tile's PV
-// and QK^T.
+// The two softmax warpgroups run independently, so while one tile's softmax
+// runs the tensor core can work on the other tile's PV and QK^T.
 #include <math.h>
 
 #include <atomic>
