@@ -321,15 +321,9 @@ def run_gpu(args, rank, world):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic",
-        "config": {
-            "workload": f"{args.workload}: B={x.B}, Hq={x.Hq}, Hkv={x.Hkv}, d={x.d}, "
-                        f"page_size={x.page_size}, kv tokens={int(x.seq_lens.sum())}, "
-                        f"pool={x.num_pages} pages; step = kv_store + paged decode",
-            "seed": args.seed,
-            "bytes_per_step": B_step,
-            "l2": "KV pool 1.3 GB > 129 MB L2: inputs larger than L2, no flush",
-            "parallelism": f"replicas x{world}",
-        },
+        "config": dict(workload_config(args, x),
+                       l2="KV pool 1.3 GB > 129 MB L2: inputs larger than L2, no flush",
+                       parallelism=f"replicas x{world}"),
         "pct_of_peak": round(100.0 * value / world / hbm_peak, 2),
         "tokens_per_s": round(world * x.B / (ms_all * 1e-3), 1),
         "roofline": {
@@ -554,27 +548,47 @@ def cpu_baseline(x, target_s=12.0):
                       f"{reps} time(s) ({nbytes} algorithmic bytes), float64 C, OpenMP over rows"}
 
 
+def workload_config(args, x):
+    """The `config` object both arms report for the decode workload x."""
+    return {
+        "workload": f"{args.workload}: B={x.B}, Hq={x.Hq}, Hkv={x.Hkv}, d={x.d}, "
+                    f"page_size={x.page_size}, kv tokens={int(x.seq_lens.sum())}, "
+                    f"pool={x.num_pages} pages; step = kv_store + paged decode",
+        "seed": args.seed,
+        "bytes_per_step": decode_bytes(x) + store_bytes(x),
+    }
+
+
 def run_reference(args):
+    """The oracle as it stands, timed on the host cores on the decode workload.
+    Each step runs the same bounded sample (the first sequences of the batch),
+    sized once so that the whole run takes about a minute whatever the step
+    count."""
     import oracle
     from synth import make_config
     oracle.build()
     x = make_config(args.workload, seed=args.seed, **batch_override(args))
     threads = oracle.max_threads()
-    per_step = max(1.0, 20.0 / max(1, args.steps + args.warmup))
+    per_step = min(2.0, 60.0 / (args.steps + args.warmup))
+    _, _, nseq = oracle_sample(x, per_step, threads)  # size the sample once
+    sub = x.subset(0, nseq)
+    nb = decode_bytes(sub) + store_bytes(sub)
     for _ in range(args.warmup):
-        oracle_sample(x, per_step, threads)
-    tot_t, tot_b, nseq = 0.0, 0, 0
+        oracle.run_inputs(sub, threads=threads, inplace=True)
+    tot_t = 0.0
     for _ in range(args.steps):
-        dt, nb, nseq = oracle_sample(x, per_step, threads)
-        tot_t += dt
-        tot_b += nb
-    value = tot_b / tot_t / 1e9
+        t = time.perf_counter()
+        oracle.run_inputs(sub, threads=threads, inplace=True)
+        tot_t += time.perf_counter() - t
+    value = args.steps * nb / tot_t / 1e9
+    config = workload_config(args, x)
+    config["sample"] = f"first {nseq} of {x.B} sequences per step"
     return {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
         "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(1e3 * tot_t / args.steps, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": f"{args.workload} (bounded samples of the step)", "seed": args.seed},
+        "config": config,
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads,
                          "kind": "oracle",
                          "sample": f"each step: kv_store + attention of the first {nseq} of "
