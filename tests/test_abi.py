@@ -107,3 +107,18 @@ def test_prefill_rejects_bad_arguments(lib):
 def test_workspace_size_is_zero_for_bad_sizes(lib):
     assert lib.pkv_decode_workspace_size(4, 12, 8, 128) == 0
     assert lib.pkv_decode_workspace_size(4, 16, 8, 96) == 0
+
+
+def test_header_is_plain_c99(tmp_path):
+    """include/pkv.h is a C header: it compiles as strict C99 with no warnings."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no gcc")
+    src = tmp_path / "use_header.c"
+    src.write_text('#include "pkv.h"\nint main(void) { return pkv_version() > 0 ? 0 : 1; }\n')
+    inc = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
+    r = subprocess.run([gcc, "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror", "-fsyntax-only",
+                        "-I", inc, str(src)], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
