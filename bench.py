@@ -374,6 +374,7 @@ def time_prefill(args, dev, stream, bf16_peak, bf16_sus, peak_kind):
     pkv.kv_store(to_dev(x.k_new, dev), to_dev(x.v_new, dev), to_dev(x.out_loc, dev), k, v,
                  dev_status=status, stream=stream)
     out = torch.empty_like(q)
+    pws = pkv.prefill_workspace(dev)
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     reps = max(5, args.steps)
     times = []
@@ -382,8 +383,8 @@ def time_prefill(args, dev, stream, bf16_peak, bf16_sus, peak_kind):
             flush.zero_()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
-            pkv.paged_prefill_attn(q, cu, k, v, pt, sl, x.scale, x.max_q_len, dev_status=status,
-                                   out=out, stream=stream)
+            pkv.paged_prefill_attn(q, cu, k, v, pt, sl, x.scale, x.max_q_len, workspace=pws,
+                                   dev_status=status, out=out, stream=stream)
             b.record(stream)
             b.synchronize()
             if i >= args.warmup:
@@ -458,13 +459,15 @@ def time_mixed_step(args, dev, stream):
     pre_max_q = int(x.new_lens[:npre].max())
     out = torch.empty_like(q)
     ws = pkv.decode_workspace(x.B - npre, x.Hq, x.Hkv, x.d, dev)
+    pws = pkv.prefill_workspace(dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
 
     def step():
         for k, v in pools:
             pkv.kv_store(kn, vn, loc, k, v, dev_status=status, stream=stream)
             pkv.paged_prefill_attn(q[:t_pre], cu[:npre + 1], k, v, pt[:npre], sl[:npre], x.scale,
-                                   pre_max_q, dev_status=status, out=out[:t_pre], stream=stream)
+                                   pre_max_q, workspace=pws, dev_status=status, out=out[:t_pre],
+                                   stream=stream)
             pkv.paged_decode_attn(q[t_pre:], k, v, pt[npre:], sl[npre:], x.scale, workspace=ws,
                                   dev_status=status, out=out[t_pre:], stream=stream)
 

@@ -81,6 +81,9 @@ typedef enum pkv_status {
 #define PKV_DEV_BAD_CUSEQ   8  /* cu_seqlens_q not monotone, not starting at 0, or new
                                   tokens beyond max_q_len / total_q_tokens */
 #define PKV_DEV_TIMEOUT    16  /* an internal pipeline wait gave up (should never happen) */
+#define PKV_DEV_BAD_WORKSPACE 32  /* prefill: the workspace counters were not zero when the
+                                     call started (never cleared, or in use by another call
+                                     at the same time); work may have been skipped */
 
 /* Human-readable name of a pkv_status value. */
 const char *pkv_status_string(int status);
@@ -206,15 +209,23 @@ pkv_status pkv_paged_decode_attn_store(const pkv_bf16 *q, const pkv_bf16 *k_new,
  *                 request r owns new tokens cu_seqlens_q[r] .. cu_seqlens_q[r+1]-1
  *   seq_lens      [batch] int32: cached prefix c_r plus new tokens n_r
  *   max_q_len     host upper bound on every n_r (sizes the launch grid)
+ *   workspace     device buffer of at least pkv_prefill_workspace_size() bytes,
+ *                 16-byte aligned, holding the call's work-queue counters.  It
+ *                 must be zero-filled once before its first use (cudaMemset);
+ *                 every call returns it to zero when its last thread block
+ *                 finishes, so it can be reused by later calls, graph replays
+ *                 included.  Calls that may run at the same time (different
+ *                 streams, or several captured calls in flight) need
+ *                 workspaces of their own.  A call that finds the counters
+ *                 not zero (a workspace never cleared, or in use by another
+ *                 call at the same time) may skip work: it raises
+ *                 PKV_DEV_BAD_WORKSPACE and its output is unspecified.
  *   out           [total_q_tokens, num_q_heads, head_dim] bf16: new token i of
  *                 request r (absolute position c_r + i) attends keys
  *                 0 .. c_r + i; accumulated in fp32, rounded to bf16
  * Other arguments as for pkv_paged_decode_attn.
- * The kernel is persistent (one thread block per SM) and hands out its work
- * through a counter pair that the library keeps in device memory: each call
- * takes the next of 256 pairs, and its last block resets the pair.  So at
- * most 256 calls may run at the same time, and a call captured in a CUDA
- * graph keeps its pair: one captured call must not run twice at once.
+ * The kernel is persistent (one thread block per SM); its blocks take their
+ * first work item by block index and the rest from the workspace counters.
  */
 pkv_status pkv_paged_prefill_attn(const pkv_bf16 *q, const int32_t *cu_seqlens_q,
                                   const pkv_bf16 *k_cache, const pkv_bf16 *v_cache,
@@ -223,7 +234,11 @@ pkv_status pkv_paged_prefill_attn(const pkv_bf16 *q, const int32_t *cu_seqlens_q
                                   int64_t total_q_tokens, int max_q_len,
                                   int num_q_heads, int num_kv_heads, int head_dim,
                                   int page_size, int64_t num_pages, float softmax_scale,
+                                  void *workspace, size_t workspace_bytes,
                                   int32_t *dev_status, pkv_bf16 *out, void *stream);
+
+/* Bytes of device workspace pkv_paged_prefill_attn needs (a small constant). */
+size_t pkv_prefill_workspace_size(void);
 
 /*
  * Size of the fixed scratch area that pkv_paged_decode_attn_noalloc uses in

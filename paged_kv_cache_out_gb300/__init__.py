@@ -8,6 +8,7 @@ from .binding import (  # noqa: F401
     DEV_BAD_PAGE,
     DEV_BAD_SEQLEN,
     DEV_BAD_SLOT,
+    DEV_BAD_WORKSPACE,
     DEV_TIMEOUT,
     PkvError,
     decode_workspace,
@@ -17,4 +18,5 @@ from .binding import (  # noqa: F401
     paged_decode_attn,
     paged_decode_attn_store,
     paged_prefill_attn,
+    prefill_workspace,
 )

@@ -20,6 +20,7 @@ _lib = None
 
 OK, EINVAL, EUNSUPPORTED, ECUDA = 0, 1, 2, 3
 DEV_BAD_SLOT, DEV_BAD_PAGE, DEV_BAD_SEQLEN, DEV_BAD_CUSEQ, DEV_TIMEOUT = 1, 2, 4, 8, 16
+DEV_BAD_WORKSPACE = 32
 
 _P = ctypes.c_void_p
 _I32, _I64, _F32, _SZ = ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
@@ -34,7 +35,8 @@ SIGNATURES = {
     "pkv_paged_decode_attn_store": ([_P, _P, _P, _P, _P, _P, _P, _I64, _P, _I32, _I32, _I32,
                                      _I32, _I32, _I64, _F32, _P, _SZ, _P, _P, _P], _I32),
     "pkv_paged_prefill_attn": ([_P, _P, _P, _P, _P, _I64, _P, _I32, _I64, _I32, _I32, _I32,
-                                _I32, _I32, _I64, _F32, _P, _P, _P], _I32),
+                                _I32, _I32, _I64, _F32, _P, _SZ, _P, _P, _P], _I32),
+    "pkv_prefill_workspace_size": ([], _SZ),
     "pkv_paged_decode_attn_noalloc": ([_P, _P, _P, _P, _I64, _P, _I32, _I32, _I32, _I32, _I32,
                                        _I64, _F32, _P, _P, _P], _I32),
 }
@@ -162,9 +164,19 @@ def paged_decode_attn_store(q, k_new, v_new, out_loc, k_cache, v_cache, page_tab
     return out
 
 
+def prefill_workspace(device=None):
+    """A zero-filled prefill workspace (the queue counters must start at zero;
+    every call leaves them at zero)."""
+    n = int(load_library().pkv_prefill_workspace_size())
+    return torch.zeros(max(n, 16), dtype=torch.uint8, device=device or "cuda")
+
+
 def paged_prefill_attn(q, cu_seqlens_q, k_cache, v_cache, page_table, seq_lens, softmax_scale,
-                       max_q_len, dev_status=None, out=None, stream=None):
-    """Ragged causal prefill: q [Tq, Hq, d] with offsets cu_seqlens_q [B+1]."""
+                       max_q_len, workspace=None, dev_status=None, out=None, stream=None):
+    """Ragged causal prefill: q [Tq, Hq, d] with offsets cu_seqlens_q [B+1].
+
+    workspace: from prefill_workspace(); calls that may overlap on the GPU
+    need separate workspaces.  Without one, a fresh zeroed one is made."""
     _bf16(q, "q"), _bf16(k_cache, "k_cache"), _bf16(v_cache, "v_cache")
     _i32(seq_lens, "seq_lens"), _i32(cu_seqlens_q, "cu_seqlens_q")
     if page_table.dtype != torch.int32 or page_table.dim() != 2 or page_table.stride(1) != 1:
@@ -176,9 +188,12 @@ def paged_prefill_attn(q, cu_seqlens_q, k_cache, v_cache, page_table, seq_lens, 
         raise ValueError("shape mismatch")
     if out is None:
         out = torch.empty_like(q)
+    if workspace is None:
+        workspace = prefill_workspace(q.device)
     st = load_library().pkv_paged_prefill_attn(
         _ptr(q), _ptr(cu_seqlens_q), _ptr(k_cache), _ptr(v_cache), _ptr(page_table),
         page_table.stride(0), _ptr(seq_lens), B, Tq, int(max_q_len), Hq, Hkv, d, ps, P,
-        float(softmax_scale), _ptr(dev_status), _ptr(out), _stream(stream))
+        float(softmax_scale), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _ptr(dev_status), _ptr(out), _stream(stream))
     _check("pkv_paged_prefill_attn", st)
     return out

@@ -12,30 +12,33 @@
 // Work item: two 128-row query tiles, A and B, of one request and one KV
 // head; a tile holds 128/G consecutive new tokens x the G query heads of that
 // KV head, so every K/V tile staged in shared memory serves 2 x 128 rows.
-// The kernel is persistent: one block per SM takes items from a queue (an
-// atomic counter) in order of decreasing work, heaviest first, so the last
-// items to finish are light ones, and the next item's Q and first K/V tiles
-// load while the current item finishes.  Roles (352 threads):
-//   warp 8      producer: takes the next item from the queue and publishes it
-//               to the other roles through a 2-slot ring; per item the Q
-//               tiles A and B, then 128-key K and V tiles through 2-stage
-//               rings, K one tile ahead of V.  Pages of >= 8 tokens come in as
-//               TMA boxes (one per page and 64-column block, 128-byte swizzle,
-//               straight into the layout the tensor core reads); smaller pages
-//               are gathered by the warp's lanes with 16-byte loads and
-//               swizzled stores.  Page ids are read in warp-wide windows, one
-//               window ahead.
-//   warps 9,10  warp 9 allocates all 512 TMEM columns (per query tile: a
-//               128x128 fp32 score buffer S, whose first 64 columns then hold
-//               P as bf16 pairs, and a 128 x head_dim fp32 output accumulator
-//               O); one lane of warp 9 + t issues the MMAs of tile t, in this
+// The kernel is persistent: one block per SM takes items in order of
+// decreasing work, heaviest first (its first item by block index, the rest
+// from a queue counter in the caller's workspace), so the last items to
+// finish are light ones, and the next item's Q and first K/V tiles load while
+// the current item finishes.  Roles (320 threads):
+//   warp 8      producer: takes the next item and publishes it to the other
+//               roles through a 2-slot ring; per item the Q tiles A and B,
+//               then 128-key K and V tiles through 2-stage rings, K one tile
+//               ahead of V.  Pages of >= 8 tokens come in as TMA boxes (one
+//               per page and 64-column block, 128-byte swizzle, straight into
+//               the layout the tensor core reads); smaller pages are gathered
+//               by the warp's lanes with 16-byte loads and swizzled stores.
+//               Page ids are read in warp-wide windows, one window ahead.
+//   warp 9      allocates all 512 TMEM columns (per query tile: a 128x128
+//               fp32 score buffer S, whose first 64 columns then hold P as
+//               bf16 pairs, and a 128 x head_dim fp32 output accumulator O)
+//               and one of its lanes issues every MMA of both tiles, in this
 //               order per key tile j:
-//                 O_t += P_t(j) V_j,  S_t(j+1) = Q_t K_(j+1)^T,
+//                 O_A += P_A(j) V_j,  S_A(j+1) = Q_A K_(j+1)^T,
+//                 O_B += P_B(j) V_j,  S_B(j+1) = Q_B K_(j+1)^T,
 //               with S from Q and K in shared memory (M=128, N=128,
 //               K=head_dim) and PV reading P from tensor memory and V from
-//               shared memory (M=128, N=head_dim, K=128).  Because the tensor
-//               core runs one block's MMAs in order, the commit of S(j+1) also
-//               tells that PV(j) has read P(j) and written O.
+//               shared memory (M=128, N=head_dim, K=128).  The tensor core
+//               runs one thread's MMAs in order, so the commit of S(j+1) also
+//               tells that PV(j) has read P(j) and written O.  (A single
+//               issuing thread keeps the tensor core at its full rate; two
+//               threads issuing at the same time slow each other down.)
 //   warps 0-3   softmax of tile A, warps 4-7 softmax of tile B: thread i of a
 //               warpgroup owns row i (TMEM lane i): reads its scores, applies
 //               the causal mask by selection, keeps a running max and sum in
@@ -45,8 +48,8 @@
 //               item reads O out of tensor memory (then frees it for the next
 //               item), normalises and stores the row.  A warp whose 32 rows
 //               are all past the request's last token does no arithmetic.
-// The two softmax warpgroups run independently, so while one tile's softmax
-// runs the tensor core can work on the other tile's PV and QK^T.
+// While one tile's softmax runs, the tensor core works on the other tile's PV
+// and QK^T, so the two tiles take turns on the tensor core.
 #include <math.h>
 
 #include <atomic>
@@ -57,25 +60,30 @@
 namespace pkv {
 namespace prefill {
 
-constexpr int kThreads = 352;
+constexpr int kThreads = 384;
 constexpr int BM = 128;  // rows of a query tile: (token, head) pairs
 constexpr int NQ = 2;    // query tiles per item
 constexpr int BN = 128;  // keys per KV tile
-constexpr int kKStages = 2, kVStages = 2;
-constexpr int kProducerWarp = 8, kMmaWarp = 9;  // warps 9 and 10 issue the MMAs of tiles A and B
-constexpr int kItemSlots = 2;                   // items published ahead of the consumers
-constexpr int kItemConsumers = 2 + 8;           // MMA warps + softmax warps
-constexpr int kRankGroups = 256;                // up to this many (token block, request) groups
-                                                // are ranked by work in the kernel
-constexpr int kSchedSlots = 256;                // queue counters for calls in flight at once
+constexpr int kKStages = 2, kVStages = 3;
+constexpr int kProducerWarp = 8, kMmaWarp = 9;  // warps 10 and 11 load K/V tiles with warp 8
+constexpr int kLoaders = 3;              // warps issuing the K/V copies (8, 10, 11)
+constexpr int kItemSlots = 2;            // items published ahead of the consumers
+constexpr int kItemConsumers = 1 + 8 + (kLoaders - 1);  // MMA, softmax and loader warps
+constexpr int kRankGroups = 256;         // up to this many (token block, request) groups
+                                         // are ranked by work in the kernel
+constexpr size_t kWorkspaceBytes = 256;  // queue counters (three used, the rest reserved)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kNegBig = -1.0e30f;
 constexpr float kRescaleLog2 = 8.0f;  // lazy rescale threshold (factor 256)
 constexpr uint32_t kTmemCols = 512;
-
-// Work-queue counters, one pair per slot: [0] next item, [1] blocks finished.
-// The last block of a call to finish puts both back to zero.
-static __device__ unsigned int g_sched[kSchedSlots][2];
+// Registers per thread: the block launches with kRegsLaunch for all 384
+// threads; then warpgroup 2 (producer, MMA issuer, loaders) gives up all but
+// kRegsLow and the two softmax warpgroups take kRegsHigh each, so that a row's
+// 128 scores and the softmax's temporaries fit without spilling.
+// 256 x kRegsHigh + 128 x kRegsLow must not exceed 384 x kRegsLaunch.
+constexpr int kRegsLaunch = 168, kRegsHigh = 208, kRegsLow = 88;
+static_assert(8 * 32 * kRegsHigh + 4 * 32 * kRegsLow <= kThreads * kRegsLaunch,
+              "register split exceeds the block's registers");
 
 template <int D>
 struct Layout {
@@ -86,8 +94,7 @@ struct Layout {
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_K = OFF_Q + NQ * Q_BYTES;
     static constexpr int OFF_V = OFF_K + kKStages * KV_BYTES;
-    static constexpr int OFF_STAGE = OFF_V + kVStages * KV_BYTES;  // output staging, 2 KB per softmax warp
-    static constexpr int OFF_BAR = OFF_STAGE + 8 * 2048;
+    static constexpr int OFF_BAR = OFF_V + kVStages * KV_BYTES;
     // qfull, qempty, kfull/kempty[kKStages], vfull/vempty[kVStages],
     // per query tile: sfull, pfull, odone, ofree; item full/empty[kItemSlots]
     static constexpr int NBARS = 2 + 2 * kKStages + 2 * kVStages + NQ * 4 + 2 * kItemSlots;
@@ -194,6 +201,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int *item_ring = misc + 1;  // [kItemSlots]: published item, -1 = no more
     volatile int *bad_flag = misc + 3;   // [kItemSlots]: a page id of that item was invalid
     volatile int *n_items_s = misc + 5;
+    volatile int *taken_s = misc + 6;    // items this block took from the queue (producer)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Lo::OFF_MISC + 32);
     int *order = reinterpret_cast<int *>(smem + Lo::OFF_RANK);
     Item *items = reinterpret_cast<Item *>(smem + Lo::OFF_ITEMS);  // the published items, decoded
@@ -221,14 +229,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (tid == 0) {
         mbar_init(BAR(B_QFULL), 1);
-        mbar_init(BAR(B_QEMPTY), NQ);  // one commit per MMA warp
+        mbar_init(BAR(B_QEMPTY), 1);  // MMA commits
         for (int s = 0; s < kKStages; ++s) {
-            mbar_init(BAR(B_KFULL(s)), 1);
-            mbar_init(BAR(B_KEMPTY(s)), NQ);
+            mbar_init(BAR(B_KFULL(s)), kLoaders);  // one arrival per loader warp (+ tx bytes)
+            mbar_init(BAR(B_KEMPTY(s)), 1);
         }
         for (int s = 0; s < kVStages; ++s) {
-            mbar_init(BAR(B_VFULL(s)), 1);
-            mbar_init(BAR(B_VEMPTY(s)), NQ);
+            mbar_init(BAR(B_VFULL(s)), kLoaders);
+            mbar_init(BAR(B_VEMPTY(s)), 1);
         }
         for (int qt = 0; qt < NQ; ++qt) {
             mbar_init(BAR(B_SFULL(qt)), 1);
@@ -242,6 +250,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         *abort_flag = 0;
         *n_items_s = 0;
+        *taken_s = 0;
         fence_mbar_init();
     }
     if (warp == kMmaWarp) {
@@ -285,80 +294,111 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t sK = smem_u32(smem + Lo::OFF_K);
     const uint32_t sV = smem_u32(smem + Lo::OFF_V);
 
-    if (warp == kProducerWarp) {
-        // ================================================================ producer
+    if (warp >= kProducerWarp) {
+    regs_decrease<kRegsLow>();
+    if (warp != kMmaWarp) {
+        // ================================================================ producer and loaders
+        // Warp 8 takes the items and publishes them, and loads the Q tiles;
+        // warps 8, 10 and 11 share the copies of every K and V tile (loader
+        // li issues boxes li, li + 3, li + 6, ...): a warp's TMA issue rate,
+        // not the copy engine, limits small boxes, so three warps issuing
+        // keep the tensor core fed where one could not.
+        const int li = warp == kProducerWarp ? 0 : warp - kMmaWarp;  // 0, 1, 2
         const uint64_t pol_kv = l2_evict_last_policy();  // K/V tiles are re-read by other blocks
         const uint64_t pol_q = l2_evict_first_policy();
         if (lane == 0) {
-            prefetch_tmap(&qmap);
+            if (li == 0) prefetch_tmap(&qmap);
             if (box_rows >= 8) {
                 prefetch_tmap(&kmap);
                 prefetch_tmap(&vmap);
             }
         }
         const int ps_mask = (1 << ps_log2) - 1;
-        const int bpt = box_rows >= 8 ? BN / box_rows : 1;  // boxes per tile (<= 16)
+        const int bpt = box_rows >= 8 ? BN / box_rows : 1;  // page boxes per tile (<= 16)
+        constexpr int NBLK = D / 64;                        // 64-column blocks of a row
         uint32_t kt = 0, vt = 0;  // K and V tiles loaded so far (ring position)
         bool ok = true;
+        bool first = true;        // the first item of a block is its block index
         Item itm;
         for (uint32_t ii = 0; ok; ++ii) {
-            // next item with work; invalid ones are flagged (and for bad
-            // lengths written as NaN) here and not published
-            int p = -1;
-            while (true) {
-                int q = 0;
-                if (lane == 0) q = static_cast<int>(atomicAdd(sched, 1u));
-                q = __shfl_sync(0xffffffffu, q, 0);
-                if (q >= n_items) break;
-                decode_item<G>(q, Hkv, B, mtiles, order, ranked, cu_seqlens, seq_lens, itm);
-                const int cu1 = itm.cu0 + itm.n;
-                if (itm.cu0 < 0 || itm.n < 0 || cu1 > Tq || (itm.r == 0 && itm.cu0 != 0) ||
-                    itm.n > max_q_len) {
-                    if (lane == 0 && dev_status) atomicOr(dev_status, PKV_DEV_BAD_CUSEQ);
-                    continue;
-                }
-                const int blk_tok0 = itm.mt * NQ * TOK;
-                if (blk_tok0 >= itm.n) continue;
-                if (itm.c < 0 || itm.L > cap) {
-                    if (lane == 0 && dev_status) atomicOr(dev_status, PKV_DEV_BAD_SEQLEN);
-                    const int blk_tok1 = min(itm.n, blk_tok0 + NQ * TOK);
-                    for (int idx = lane; idx < (blk_tok1 - blk_tok0) * G * D; idx += 32) {
-                        const int t = blk_tok0 + idx / (G * D);
-                        const int rem = idx % (G * D);
-                        out[((int64_t)(itm.cu0 + t) * Hq + (int64_t)itm.g * G) * D + rem] =
-                            __float2bfloat16_rn(__int_as_float(0x7fc00000));
-                    }
-                    continue;
-                }
-                p = q;
-                break;
-            }
-            // publish it (or the end) to the MMA and softmax warps
             const int slot = ii % kItemSlots;
-            if (ii >= kItemSlots &&
-                !mbar_wait_warp(BAR(B_IEMPTY(slot)), ((ii / kItemSlots) & 1) ^ 1, abort_flag, dev_status))
-                break;
-            if (lane == 0) {
-                item_ring[slot] = p;
-                bad_flag[slot] = 0;
-                if (p >= 0) items[slot] = itm;
-                mbar_arrive(BAR(B_IFULL(slot)));
+            int p = -1;
+            if (li == 0) {
+                // next item with work; invalid ones are flagged (and for bad
+                // lengths written as NaN) here and not published
+                while (true) {
+                    int q = static_cast<int>(blockIdx.x);
+                    if (!first) {
+                        if (lane == 0) q = static_cast<int>(gridDim.x + atomicAdd(sched, 1u));
+                        q = __shfl_sync(0xffffffffu, q, 0);
+                    }
+                    first = false;
+                    if (q >= n_items) break;
+                    if (lane == 0) *taken_s += 1;
+                    decode_item<G>(q, Hkv, B, mtiles, order, ranked, cu_seqlens, seq_lens, itm);
+                    const int cu1 = itm.cu0 + itm.n;
+                    if (itm.cu0 < 0 || itm.n < 0 || cu1 > Tq || (itm.r == 0 && itm.cu0 != 0) ||
+                        itm.n > max_q_len) {
+                        if (lane == 0 && dev_status) atomicOr(dev_status, PKV_DEV_BAD_CUSEQ);
+                        continue;
+                    }
+                    const int blk_tok0 = itm.mt * NQ * TOK;
+                    if (blk_tok0 >= itm.n) continue;
+                    if (itm.c < 0 || itm.L > cap) {
+                        if (lane == 0 && dev_status) atomicOr(dev_status, PKV_DEV_BAD_SEQLEN);
+                        const int blk_tok1 = min(itm.n, blk_tok0 + NQ * TOK);
+                        for (int idx = lane; idx < (blk_tok1 - blk_tok0) * G * D; idx += 32) {
+                            const int t = blk_tok0 + idx / (G * D);
+                            const int rem = idx % (G * D);
+                            out[((int64_t)(itm.cu0 + t) * Hq + (int64_t)itm.g * G) * D + rem] =
+                                __float2bfloat16_rn(__int_as_float(0x7fc00000));
+                        }
+                        continue;
+                    }
+                    p = q;
+                    break;
+                }
+                // publish it (or the end) to the other roles
+                if (ii >= kItemSlots &&
+                    !mbar_wait_warp(BAR(B_IEMPTY(slot)), ((ii / kItemSlots) & 1) ^ 1, abort_flag, dev_status))
+                    break;
+                if (lane == 0) {
+                    item_ring[slot] = p;
+                    bad_flag[slot] = 0;
+                    if (p >= 0) items[slot] = itm;
+                    mbar_arrive(BAR(B_IFULL(slot)));
+                }
+                __syncwarp();
+            } else {
+                if (!mbar_wait_warp(BAR(B_IFULL(slot)), (ii / kItemSlots) & 1, abort_flag, dev_status)) break;
+                p = item_ring[slot];
+                if (p >= 0) itm = items[slot];
             }
-            __syncwarp();
             if (p < 0) break;
 
             const int32_t *prow = page_table + (int64_t)itm.r * pt_stride;
             const int L = itm.L, g = itm.g;
-            // page ids in warp-wide windows of 32 boxes, the next window loaded ahead
+            // page ids in warp-wide windows of 32 page boxes, the next window loaded ahead
             auto load_window = [&](int w) -> int {
                 const int key = (32 * w + lane) * box_rows;
                 return (box_rows >= 8 && key < L) ? prow[key >> ps_log2] : 0;
             };
             int w_cur = 0;
             int pg_cur = load_window(0), pg_nxt = load_window(1);
+            // page id of page box pb of tile j (lanes past the tile's boxes get
+            // a neighbour's id, unused)
+            auto page_of = [&](int j, int pb) -> int {
+                const int b0 = j * bpt;
+                if ((b0 >> 5) != w_cur) {
+                    w_cur = b0 >> 5;
+                    pg_cur = pg_nxt;
+                    pg_nxt = load_window(w_cur + 1);
+                }
+                return __shfl_sync(0xffffffffu, pg_cur, (b0 + min(pb, bpt - 1)) & 31);
+            };
             // one K or V tile (tile j of the item, ring position t): wait for
-            // its slot, then TMA boxes (or gather)
-            auto load_tile = [&](int kv, int j, uint32_t t, int pg_tile) -> bool {
+            // its slot, then this loader's share of the TMA boxes (or gather)
+            auto load_tile = [&](int kv, int j, uint32_t t) -> bool {
                 const int ns = kv ? kVStages : kKStages;
                 const int s = t % ns;
                 const uint32_t ph = (t / ns) & 1;
@@ -370,28 +410,34 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (t >= static_cast<uint32_t>(ns) && !mbar_wait_warp(empty, ph ^ 1, abort_flag, dev_status))
                     return false;
                 if (box_rows >= 8) {
-                    const int nbox = (nkeys + box_rows - 1) / box_rows;  // <= 16
-                    const bool bad = lane < nbox && (pg_tile < 0 || pg_tile >= num_pages);
-                    const int nbad = __popc(__ballot_sync(0xffffffffu, bad));
+                    const int nbox = (nkeys + box_rows - 1) / box_rows;  // page boxes, <= 16
+                    const int b = li + kLoaders * lane;                  // this lane's box
+                    const int pb = b / NBLK, blk = b % NBLK;
+                    const int pg = page_of(j, pb);
+                    const bool mine = pb < nbox;
+                    // a page id outside the pool is flagged; its box is read from
+                    // a row before the pool, which the copy engine fills with zeros
+                    const bool bad = mine && (pg < 0 || pg >= num_pages);
+                    if (__any_sync(0xffffffffu, bad) && lane == 0) bad_flag[slot] = 1;
                     if (lane == 0) {
-                        if (nbad) bad_flag[slot] = 1;
-                        mbar_arrive_expect_tx(
-                            full, static_cast<uint32_t>((nbox - nbad) * (D / 64) * box_rows * 128));
+                        if (li == 0)
+                            mbar_arrive_expect_tx(full,
+                                                  static_cast<uint32_t>(nbox * NBLK * box_rows * 128));
+                        else
+                            mbar_arrive(full);
+                    }
+                    if (mine) {
+                        const int kk = key0 + pb * box_rows;
+                        const int row = bad ? -box_rows : (pg << ps_log2) + (kk & ps_mask);
+                        tma_load_3d(dst + blk * Lo::KBLK + pb * box_rows * 128, kv ? &vmap : &kmap, full,
+                                    blk * 64, g, row, pol_kv);
                     }
                     __syncwarp();
-                    if (lane < nbox && !bad) {
-                        const int kk = key0 + lane * box_rows;
-                        const int row = (pg_tile << ps_log2) + (kk & ps_mask);
-#pragma unroll
-                        for (int blk = 0; blk < D / 64; ++blk)
-                            tma_load_3d(dst + blk * Lo::KBLK + lane * box_rows * 128, kv ? &vmap : &kmap,
-                                        full, blk * 64, g, row, pol_kv);
-                    }
                 } else {
                     // small pages: gather 16-byte chunks, swizzle, zero rows past the sequence
                     const __nv_bfloat16 *base = kv ? v_cache : k_cache;
                     bool bad = false;
-                    for (int idx = lane; idx < BN * (D / 8); idx += 32) {
+                    for (int idx = li * 32 + lane; idx < BN * (D / 8); idx += kLoaders * 32) {
                         const int key = idx / (D / 8), ch = idx % (D / 8);
                         uint4 val = make_uint4(0u, 0u, 0u, 0u);
                         if (key < nkeys) {
@@ -415,15 +461,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 return true;
             };
-            auto page_of_tile = [&](int j) -> int {
-                const int b0 = j * bpt;
-                if ((b0 >> 5) != w_cur) {
-                    w_cur = b0 >> 5;
-                    pg_cur = pg_nxt;
-                    pg_nxt = load_window(w_cur + 1);
-                }
-                return __shfl_sync(0xffffffffu, pg_cur, (b0 + (lane % bpt)) & 31);
-            };
             // K(0) first: it needs only a free K slot; the Q tiles wait until
             // the previous item's QK^T MMAs have read the Q buffer.  Until then
             // the Q tiles and the first K and V tiles are prefetched into L2.
@@ -435,95 +472,87 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int qt = 0; qt < NQ; ++qt)
 #pragma unroll
-                        for (int blk = 0; blk < D / 64; ++blk)
+                        for (int blk = 0; blk < NBLK; ++blk)
                             tma_load_3d(sQ + qt * Lo::Q_BYTES + blk * Lo::BLK, &qmap, BAR(B_QFULL),
                                         blk * 64, g * G, itm.cu0 + (qt ? itm.tbeg[1] : itm.tbeg[0]), pol_q);
                 }
                 __syncwarp();
             };
-            if (ii == 0) load_q();
-            int pg_prev = page_of_tile(0);
-            if (ii > 0 && lane == 0) {
+            if (li == 0 && ii == 0) load_q();
+            if (li == 0 && ii > 0) {
+                if (lane == 0) {
 #pragma unroll
-                for (int qt = 0; qt < NQ; ++qt)
+                    for (int qt = 0; qt < NQ; ++qt)
 #pragma unroll
-                    for (int blk = 0; blk < D / 64; ++blk)
-                        tma_prefetch_3d(&qmap, blk * 64, g * G, itm.cu0 + itm.tbeg[qt]);
-            }
-            if (box_rows >= 8) {
-                const int nbox0 = (min(BN, L) + box_rows - 1) / box_rows;
-                if (lane < nbox0 && pg_prev >= 0 && pg_prev < num_pages) {
-                    const int row = pg_prev << ps_log2;  // tile 0 starts at key 0: box offset (lane * box_rows) & ps_mask
+                        for (int blk = 0; blk < NBLK; ++blk)
+                            tma_prefetch_3d(&qmap, blk * 64, g * G, itm.cu0 + itm.tbeg[qt]);
+                }
+                if (box_rows >= 8) {
+                    const int nbox0 = (min(BN, L) + box_rows - 1) / box_rows;
+                    const int pg0 = page_of(0, lane);
+                    if (lane < nbox0 && pg0 >= 0 && pg0 < num_pages) {
+                        const int row = (pg0 << ps_log2) + ((lane * box_rows) & ps_mask);
 #pragma unroll
-                    for (int blk = 0; blk < D / 64; ++blk) {
-                        tma_prefetch_3d(&kmap, blk * 64, g, row + ((lane * box_rows) & ps_mask));
-                        tma_prefetch_3d(&vmap, blk * 64, g, row + ((lane * box_rows) & ps_mask));
+                        for (int blk = 0; blk < NBLK; ++blk) {
+                            tma_prefetch_3d(&kmap, blk * 64, g, row);
+                            tma_prefetch_3d(&vmap, blk * 64, g, row);
+                        }
                     }
                 }
             }
-            ok = load_tile(0, 0, kt, pg_prev);
-            if (ok && ii > 0) {
+            ok = load_tile(0, 0, kt);
+            if (ok && li == 0 && ii > 0) {
                 ok = mbar_wait_warp(BAR(B_QEMPTY), (ii - 1) & 1, abort_flag, dev_status);
                 if (ok) load_q();
             }
             if (!ok) break;
-            // K runs one tile ahead of V: K(j+1) is needed right after PV(j)
+            // in the order the MMAs need them: V(j) for PV(j), then K(j+1) for
+            // the QK^T that follows it (K runs one tile ahead of V)
             for (int j = 0; ok && j < itm.n_kt; ++j) {
-                const int pg_j = pg_prev;
-                if (j + 1 < itm.n_kt) {
-                    pg_prev = page_of_tile(j + 1);
-                    ok = load_tile(0, j + 1, kt + j + 1, pg_prev);
-                }
-                ok = ok && load_tile(1, j, vt + j, pg_j);
+                ok = load_tile(1, j, vt + j);
+                if (ok && j + 1 < itm.n_kt) ok = load_tile(0, j + 1, kt + j + 1);
             }
             kt += itm.n_kt;
             vt += itm.n_kt;
+            if (ok && li > 0) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(BAR(B_IEMPTY(slot)));
+            }
         }
-    } else if (warp >= kMmaWarp) {
-        // ================================================================ MMA issuers
-        // Warp 9 + qt issues the MMAs of query tile qt, so one tile's issue never
-        // waits behind the other's.  Both warps step through every key tile of
-        // every item to release the K and V slots (count NQ) in phase, and both
-        // take every item's Q (also when their tile has no rows).
-        const int qt = warp - kMmaWarp;
+    } else if (warp == kMmaWarp) {
+        // ================================================================ MMA issuer
+        // One lane issues the MMAs of both query tiles in a fixed order, so a
+        // tile's PV and next QK^T run on the tensor core while the other
+        // tile's softmax runs.  The K and V slots are released by commits
+        // after both tiles' MMAs that read them.  The whole warp runs the
+        // issue code and an elected lane issues (see elect_one).
         constexpr uint32_t idesc_s = instr_desc(BM, BN, false);
         constexpr uint32_t idesc_o = instr_desc(BM, D, true);
-        auto issue_s = [&](uint32_t t) {  // S(qt) = Q(qt) K^T; K tile at ring position t
+        auto issue_s = [&](int qt, uint32_t t) {  // S(qt) = Q(qt) K^T; K tile at ring position t
             const uint32_t kb = sK + (t % kKStages) * Lo::KV_BYTES;
             const uint32_t qb = sQ + qt * Lo::Q_BYTES;
-            tc_fence_after();
-            if (lane == 0) {
+            const uint32_t leader = elect_one();
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t qoff = (kk >> 2) * Lo::BLK + (kk & 3) * 32;
-                    const uint32_t koff = (kk >> 2) * Lo::KBLK + (kk & 3) * 32;
-                    umma_bf16_ss(tm_s(qt), smem_desc(qb + qoff, 16, 1024),
-                                 smem_desc(kb + koff, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
-                }
-                umma_commit(BAR(B_SFULL(qt)));
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t qoff = (kk >> 2) * Lo::BLK + (kk & 3) * 32;
+                const uint32_t koff = (kk >> 2) * Lo::KBLK + (kk & 3) * 32;
+                umma_bf16_ss_if(tm_s(qt), smem_desc(qb + qoff, 16, 1024), smem_desc(kb + koff, 16, 1024),
+                                idesc_s, kk > 0 ? 1u : 0u, leader);
             }
-            __syncwarp();
+            umma_commit_if(BAR(B_SFULL(qt)), leader);
         };
-        auto issue_pv = [&](uint32_t t, bool acc) {  // O(qt) += P(qt) V; P in TMEM, V at ring position t
+        auto issue_pv = [&](int qt, uint32_t t, bool acc) {  // O(qt) += P(qt) V; V at ring position t
             const uint32_t vb = sV + (t % kVStages) * Lo::KV_BYTES;
-            tc_fence_after();
-            if (lane == 0) {
+            const uint32_t leader = elect_one();
 #pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk)
-                    umma_bf16_ts(tm_o(qt), tm_s(qt) + kk * 8,
-                                 smem_desc(vb + kk * 16 * 128, Lo::KBLK, 1024), idesc_o,
-                                 (acc || kk > 0) ? 1u : 0u);
-                umma_commit(BAR(B_ODONE(qt)));
-            }
-            __syncwarp();
+            for (int kk = 0; kk < BN / 16; ++kk)
+                umma_bf16_ts_if(tm_o(qt), tm_s(qt) + kk * 8, smem_desc(vb + kk * 16 * 128, Lo::KBLK, 1024),
+                                idesc_o, (acc || kk > 0) ? 1u : 0u, leader);
         };
-        auto commit = [&](uint32_t bar) {
-            if (lane == 0) umma_commit(bar);
-            __syncwarp();
-        };
-        uint32_t kt = 0, vt = 0;  // ring positions of the current item's K(0) and V(0)
-        uint32_t pc = 0;          // P tiles consumed by this warp (all items)
-        uint32_t wk = 0;          // items in which this tile had rows
+        auto commit = [&](uint32_t bar) { umma_commit_if(bar, elect_one()); };
+        uint32_t kt = 0, vt = 0;        // ring positions of the current item's K(0) and V(0)
+        uint32_t pc[NQ] = {0u, 0u};     // P tiles consumed per query tile (all items)
+        uint32_t wk[NQ] = {0u, 0u};     // items in which the query tile had rows
         bool ok = true;
         for (uint32_t ii = 0; ok; ++ii) {
             const int slot = ii % kItemSlots;
@@ -531,12 +560,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int p = item_ring[slot];
             if (p < 0) break;
             const Item &itm = items[slot];
-            const int my_kt = qt ? itm.nkt[1] : itm.nkt[0], n_kt = itm.n_kt, L = itm.L;
+            const int nk[NQ] = {itm.nkt[0], itm.nkt[1]};
+            const int n_kt = itm.n_kt, L = itm.L;
             ok = mbar_wait_warp(BAR(B_QFULL), ii & 1, abort_flag, dev_status) &&
                  mbar_wait_warp(BAR(B_KFULL(kt % kKStages)), (kt / kKStages) & 1, abort_flag, dev_status);
             if (!ok) break;
-            if (my_kt > 0) issue_s(kt);
-            if (my_kt <= 1) commit(BAR(B_QEMPTY));  // this warp's QK^T MMAs of the item are issued
+            tc_fence_after();
+#pragma unroll
+            for (int t = 0; t < NQ; ++t)
+                if (nk[t] > 0) issue_s(t, kt);
+            if (n_kt <= 1) commit(BAR(B_QEMPTY));  // every QK^T MMA of the item is issued
             commit(BAR(B_KEMPTY(kt % kKStages)));
             for (int j = 0; j < n_kt; ++j) {
                 const uint32_t tv = vt + j;
@@ -545,64 +578,83 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ok = false;
                     break;
                 }
-                if (j < my_kt) {
-                    if (j == n_kt - 1 && (j + 1) * BN > L) {
-                        // keys past the sequence end hold stale pool data (maybe NaN):
-                        // zero those V rows so that P = 0 there contributes exactly 0
-                        // (both MMA warps write the same zeros before their own PV)
-                        const uint32_t vb = sV + s * Lo::KV_BYTES;
-                        const int first = L - j * BN;
-                        for (int idx = lane; idx < (BN - first) * (D / 8); idx += 32) {
-                            const int key = first + idx / (D / 8), ch = idx % (D / 8);
-                            *reinterpret_cast<uint4 *>(smem + (vb - smem_u32(smem)) +
-                                                       swz_offset(key, ch, BN)) = make_uint4(0u, 0u, 0u, 0u);
-                        }
-                        fence_proxy_async_smem();
-                        __syncwarp();
+                if (j == n_kt - 1 && (j + 1) * BN > L) {
+                    // keys past the sequence end hold stale pool data (maybe NaN):
+                    // zero those V rows so that P = 0 there contributes exactly 0
+                    const uint32_t vb = sV + s * Lo::KV_BYTES;
+                    const int first_dead = L - j * BN;
+                    for (int idx = lane; idx < (BN - first_dead) * (D / 8); idx += 32) {
+                        const int key = first_dead + idx / (D / 8), ch = idx % (D / 8);
+                        *reinterpret_cast<uint4 *>(smem + (vb - smem_u32(smem)) +
+                                                   swz_offset(key, ch, BN)) = make_uint4(0u, 0u, 0u, 0u);
                     }
-                    if (!mbar_wait_warp(BAR(B_PFULL(qt)), pc & 1, abort_flag, dev_status)) {
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                }
+                const uint32_t tk = kt + j + 1;
+                bool k_ready = false;
+#pragma unroll
+                for (int t = 0; t < NQ; ++t) {
+                    if (!ok || j >= nk[t]) continue;
+                    if (!mbar_wait_warp(BAR(B_PFULL(t)), pc[t] & 1, abort_flag, dev_status)) {
                         ok = false;
                         break;
                     }
-                    ++pc;
+                    ++pc[t];
                     // the first PV of an item overwrites O: the previous item's
                     // output must have been read out of tensor memory
-                    if (j == 0 && wk > 0 &&
-                        !mbar_wait_warp(BAR(B_OFREE(qt)), (wk - 1) & 1, abort_flag, dev_status)) {
+                    if (j == 0 && wk[t] > 0 &&
+                        !mbar_wait_warp(BAR(B_OFREE(t)), (wk[t] - 1) & 1, abort_flag, dev_status)) {
                         ok = false;
                         break;
                     }
-                    issue_pv(tv, j > 0);
+                    tc_fence_after();
+                    issue_pv(t, tv, j > 0);
+                    if (j == nk[t] - 1) commit(BAR(B_ODONE(t)));
+                    if (j + 1 < nk[t]) {
+                        if (!k_ready) {
+                            if (!mbar_wait_warp(BAR(B_KFULL(tk % kKStages)), (tk / kKStages) & 1,
+                                                abort_flag, dev_status)) {
+                                ok = false;
+                                break;
+                            }
+                            k_ready = true;
+                            tc_fence_after();
+                        }
+                        issue_s(t, tk);
+                    }
                 }
+                if (!ok) break;
                 commit(BAR(B_VEMPTY(s)));
                 if (j + 1 < n_kt) {
-                    const uint32_t tk = kt + j + 1;
-                    if (!mbar_wait_warp(BAR(B_KFULL(tk % kKStages)), (tk / kKStages) & 1, abort_flag,
-                                        dev_status)) {
+                    if (!k_ready && !mbar_wait_warp(BAR(B_KFULL(tk % kKStages)), (tk / kKStages) & 1,
+                                                    abort_flag, dev_status)) {
                         ok = false;
                         break;
                     }
-                    if (j + 1 < my_kt) {
-                        issue_s(tk);
-                        if (j + 1 == my_kt - 1) commit(BAR(B_QEMPTY));
-                    }
+                    if (j + 1 == n_kt - 1) commit(BAR(B_QEMPTY));
                     commit(BAR(B_KEMPTY(tk % kKStages)));
                 }
             }
             kt += n_kt;
             vt += n_kt;
-            if (my_kt > 0) ++wk;
+#pragma unroll
+            for (int t = 0; t < NQ; ++t)
+                if (nk[t] > 0) ++wk[t];
             if (ok) {
                 __syncwarp();
                 if (lane == 0) mbar_arrive(BAR(B_IEMPTY(slot)));
             }
         }
+    }
     } else {
         // ================================================================ softmax
+        regs_increase<kRegsHigh>();
         const int qt = warp >> 2;                  // query tile of this warpgroup
         const int row = tid & 127;                 // TMEM lane == tile row
         const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
         uint32_t sc = 0;                  // S tiles consumed by this warpgroup (all items)
+        uint32_t od = 0;                  // items in which this tile had rows
         bool ok = true;
         for (uint32_t ii = 0; ok; ++ii) {
             const int slot = ii % kItemSlots;
@@ -630,33 +682,38 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tmem_ld_32cols(tm_s(qt) + lane_off + cc * 32, sv + cc * 32);
                     tmem_wait_ld();
                     // causal mask by selection (-inf), only on tiles that cross some
-                    // row's limit (a warp-uniform branch)
+                    // valid row's limit (a warp-uniform branch).  Rows past the
+                    // request's last token are not masked: their scores are never
+                    // used (their output is not stored, and each row of P only
+                    // feeds the same row of O), so a warp holding such rows does
+                    // not pay for masking on every tile.
                     const int key0 = j * BN;
-                    if (__any_sync(0xffffffffu, !row_valid || key0 + BN - 1 > lim)) {
-                        const int nvalid = row_valid ? lim - key0 + 1 : 0;  // keys kept in this row
+                    const int nvalid = row_valid ? lim - key0 + 1 : BN;  // keys kept in this row
+                    if (__any_sync(0xffffffffu, nvalid < BN)) {
 #pragma unroll
                         for (int i = 0; i < BN; ++i)
                             if (i >= nvalid) sv[i] = __float_as_uint(-INFINITY);
                     }
+                    // the row max, then p = 2^(s*scale*log2e - m_ref) on the SFU, packed
+                    // to bf16 pairs and written 32 keys at a time into tensor memory
+                    // over the S columns already read (keys 32cc.. -> columns 16cc..)
                     float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
                     for (int i = 0; i < BN; i += 2)
                         mx4[(i >> 1) & 3] =
                             fmax3(mx4[(i >> 1) & 3], __uint_as_float(sv[i]), __uint_as_float(sv[i + 1]));
                     const float mt_max = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * scale_log2;
-                    const bool need = (j == 0) ? false : (mt_max > m_ref + kRescaleLog2);
+                    const bool need = (j > 0) && row_valid && (mt_max > m_ref + kRescaleLog2);
                     const bool warp_need = __any_sync(0xffffffffu, need);
                     float alpha = 1.f;
                     if (j == 0) {
                         m_ref = fmaxf(mt_max, kNegBig);  // stays finite for rows with no key
+                        l_sum = 0.f;
                     } else if (warp_need) {
                         const float mn = fmaxf(m_ref, mt_max);
                         alpha = ex2(m_ref - mn);
                         m_ref = mn;
                     }
-                    // p = 2^(s*scale*log2e - m_ref) on the SFU, packed to bf16 pairs and
-                    // written 32 keys at a time into tensor memory over the S columns
-                    // already read (keys 32cc.. -> columns 16cc..)
                     const float neg_m = -m_ref;
                     float rs[4] = {0.f, 0.f, 0.f, 0.f};  // two packed pairs of partial sums
 #pragma unroll
@@ -696,20 +753,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (!ok) break;
             if (my_kt > 0) {
-                ok = mbar_wait_warp(BAR(B_ODONE(qt)), (sc + my_kt - 1) & 1, abort_flag, dev_status);
+                ok = mbar_wait_warp(BAR(B_ODONE(qt)), od & 1, abort_flag, dev_status);
+                ++od;
                 if (!ok) break;
                 tc_fence_after();
                 // the output row out of tensor memory 32 columns at a time,
-                // normalised and packed to bf16; each warp passes its 32 rows'
-                // 64-byte pieces through shared memory so that the stores to
-                // global memory are whole 64-byte runs (8 rows per instruction)
-                // instead of 16 bytes from each of 32 rows
+                // normalised, packed to bf16 and stored by its own thread in
+                // 32-byte pieces (whole sectors)
                 const bool poison = (bad_flag[slot] != 0) || (*abort_flag != 0);
                 const float inv = row_valid ? 1.f / l_sum : 0.f;
-                const uint32_t stage = smem_u32(smem + Lo::OFF_STAGE) + warp * 2048;
-                const int tbeg_q = qt ? itm.tbeg[1] : itm.tbeg[0];
-                const int tend_q = qt ? itm.tend[1] : itm.tend[0];
-                const int64_t out_row0 = (int64_t)itm.cu0 * Hq + (int64_t)itm.g * G;
+                const int64_t out_row = ((int64_t)(itm.cu0 + tok) * Hq + (int64_t)itm.g * G + row % G) * D;
                 if (warp_live) {
 #pragma unroll
                     for (int cc = 0; cc < D / 32; ++cc) {
@@ -722,23 +775,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                             pk[e / 2] = poison ? 0x7fc07fc0u  // two bf16 NaNs
                                                : pack_bf16x2(__uint_as_float(ov[e]) * inv,
                                                              __uint_as_float(ov[e + 1]) * inv);
-                        // row `lane`, 16-byte piece q at (q ^ (lane / 2 % 4)): conflict-free
-#pragma unroll
-                        for (int q = 0; q < 4; ++q)
-                            sts128(stage + lane * 64 + ((q ^ ((lane >> 1) & 3)) << 4),
-                                   make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]));
-                        __syncwarp();
-#pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            const int rl = 8 * k + (lane >> 2), q = lane & 3;
-                            const uint4 v = lds128(stage + rl * 64 + ((q ^ ((rl >> 1) & 3)) << 4));
-                            const int rt = (warp & 3) * 32 + rl;  // tile row
-                            const int t = tbeg_q + rt / G;
-                            if (t < tend_q)
-                                reinterpret_cast<uint4 *>(
-                                    out + (out_row0 + (int64_t)t * Hq + rt % G) * D + cc * 32)[q] = v;
+                        if (row_valid) {
+                            st_global_32B(out + out_row + cc * 32, pk);
+                            st_global_32B(out + out_row + cc * 32 + 16, pk + 8);
                         }
-                        __syncwarp();
                     }
                 }
                 tc_fence_before();
@@ -753,7 +793,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
     // all roles meet here, then the TMEM is freed and the queue counters of
-    // this call are reset by the last block to finish
+    // this call are reset by the last block to finish.  Every block adds the
+    // number of items it took to a third counter before it counts itself
+    // finished, so the last block sees exactly n_items there when the call
+    // started from zeroed counters; anything else (items skipped or taken
+    // twice) means the counters were shared or not cleared.
     tc_fence_before();
     __syncthreads();
     if (warp == kMmaWarp) {
@@ -761,36 +805,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_dealloc(tmem, kTmemCols);
     }
     if (tid == 0) {
+        atomicAdd(sched + 2, static_cast<unsigned int>(*taken_s));
         __threadfence();
         if (atomicAdd(sched + 1, 1u) == gridDim.x - 1) {
+            __threadfence();
+            const unsigned int taken = *reinterpret_cast<volatile unsigned int *>(sched + 2);
+            if (dev_status && taken != static_cast<unsigned int>(n_items) &&
+                (*reinterpret_cast<volatile int32_t *>(dev_status) & PKV_DEV_TIMEOUT) == 0)
+                atomicOr(dev_status, PKV_DEV_BAD_WORKSPACE);
             sched[0] = 0;
             sched[1] = 0;
+            sched[2] = 0;
             __threadfence();
         }
     }
-}
-
-// Queue counters for this call: a slot of g_sched on the current device, taken
-// round-robin, so calls in flight at the same time (up to kSchedSlots of
-// them) use different counters.  The device address of g_sched is looked up
-// once per device.
-static unsigned int *sched_counters() {
-    static std::mutex mu;
-    static unsigned int *base[64] = {};
-    static std::atomic<unsigned int> next{0};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-    unsigned int *b = nullptr;
-    {
-        std::lock_guard<std::mutex> lk(mu);
-        if (!base[dev]) {
-            void *p = nullptr;
-            if (cudaGetSymbolAddress(&p, g_sched) != cudaSuccess || !p) return nullptr;
-            base[dev] = static_cast<unsigned int *>(p);
-        }
-        b = base[dev];
-    }
-    return b + 2 * (next.fetch_add(1u) % kSchedSlots);
 }
 
 template <int D, int G>
@@ -812,8 +840,8 @@ template <int D, int G>
 static pkv_status launch(const pkv_bf16 *q, const int32_t *cu, const pkv_bf16 *k_cache,
                          const pkv_bf16 *v_cache, const int32_t *page_table, int64_t pt_stride,
                          const int32_t *seq_lens, int B, int64_t Tq, int max_q_len, int Hkv,
-                         int page_size, int64_t num_pages, float scale, int32_t *dev_status,
-                         pkv_bf16 *out, cudaStream_t stream) {
+                         int page_size, int64_t num_pages, float scale, unsigned int *sched,
+                         int32_t *dev_status, pkv_bf16 *out, cudaStream_t stream) {
     pkv_host::DeviceInfo dev;
     if (!pkv_host::current_device(&dev)) return PKV_ECUDA;
     if (!prepare<D, G>(dev)) return PKV_ECUDA;
@@ -837,8 +865,6 @@ static pkv_status launch(const pkv_bf16 *q, const int32_t *cu, const pkv_bf16 *k
     const int64_t items = static_cast<int64_t>(mtiles) * B * Hkv;
     if (items == 0) return PKV_OK;
     if (items > 0x7fffffffll) return PKV_EUNSUPPORTED;
-    unsigned int *sched = sched_counters();
-    if (!sched) return PKV_ECUDA;
     // persistent: one block per SM (fewer when there are fewer items)
     const int grid = items < dev.sm_count ? static_cast<int>(items) : dev.sm_count;
     prefill_kernel<D, G><<<static_cast<unsigned>(grid), kThreads, Layout<D>::bytes(), stream>>>(
@@ -852,6 +878,8 @@ static pkv_status launch(const pkv_bf16 *q, const int32_t *cu, const pkv_bf16 *k
 }  // namespace prefill
 }  // namespace pkv
 
+extern "C" size_t pkv_prefill_workspace_size(void) { return pkv::prefill::kWorkspaceBytes; }
+
 extern "C" pkv_status pkv_paged_prefill_attn(const pkv_bf16 *q, const int32_t *cu_seqlens_q,
                                              const pkv_bf16 *k_cache, const pkv_bf16 *v_cache,
                                              const int32_t *page_table, int64_t page_table_stride,
@@ -859,6 +887,7 @@ extern "C" pkv_status pkv_paged_prefill_attn(const pkv_bf16 *q, const int32_t *c
                                              int64_t total_q_tokens, int max_q_len,
                                              int num_q_heads, int num_kv_heads, int head_dim,
                                              int page_size, int64_t num_pages, float softmax_scale,
+                                             void *workspace, size_t workspace_bytes,
                                              int32_t *dev_status, pkv_bf16 *out, void *stream) {
     using namespace pkv::prefill;
     if (batch < 0 || total_q_tokens < 0 || max_q_len < 0 || num_q_heads <= 0 || num_kv_heads <= 0 ||
@@ -867,15 +896,17 @@ extern "C" pkv_status pkv_paged_prefill_attn(const pkv_bf16 *q, const int32_t *c
     if (num_q_heads % num_kv_heads != 0) return PKV_EINVAL;
     if (!(softmax_scale == softmax_scale)) return PKV_EINVAL;
     if (batch == 0 || total_q_tokens == 0 || max_q_len == 0) return PKV_OK;
-    if (!q || !cu_seqlens_q || !k_cache || !v_cache || !page_table || !seq_lens || !out)
+    if (!q || !cu_seqlens_q || !k_cache || !v_cache || !page_table || !seq_lens || !out ||
+        !workspace)
         return PKV_EINVAL;
     const int G = num_q_heads / num_kv_heads;
     if (head_dim != 64 && head_dim != 128) return PKV_EUNSUPPORTED;
     if (G != 1 && G != 2 && G != 4 && G != 8) return PKV_EUNSUPPORTED;
     if ((page_size & (page_size - 1)) != 0 || page_size > 256) return PKV_EUNSUPPORTED;
     if (!pkv_host::aligned16(q) || !pkv_host::aligned16(k_cache) || !pkv_host::aligned16(v_cache) ||
-        !pkv_host::aligned16(out))
+        !pkv_host::aligned16(out) || !pkv_host::aligned16(workspace))
         return PKV_EINVAL;
+    if (workspace_bytes < kWorkspaceBytes) return PKV_EINVAL;
     if (num_pages * page_size > 0x7fffffffll || total_q_tokens > 0x7fffffffll)
         return PKV_EUNSUPPORTED;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -883,7 +914,8 @@ extern "C" pkv_status pkv_paged_prefill_attn(const pkv_bf16 *q, const int32_t *c
     if (head_dim == DD && G == GG)                                                                 \
         return launch<DD, GG>(q, cu_seqlens_q, k_cache, v_cache, page_table, page_table_stride,    \
                               seq_lens, batch, total_q_tokens, max_q_len, num_kv_heads, page_size, \
-                              num_pages, softmax_scale, dev_status, out, st);
+                              num_pages, softmax_scale, static_cast<unsigned int *>(workspace), \
+                              dev_status, out, st);
     PKV_PREFILL_CASE(128, 1)
     PKV_PREFILL_CASE(128, 2)
     PKV_PREFILL_CASE(128, 4)

@@ -37,6 +37,7 @@ class Run:
         self.seq_lens = to_dev(x.seq_lens)
         self.cu = to_dev(x.cu_seqlens_q)
         self.status = torch.zeros(1, dtype=torch.int32, device=dev())
+        self.pws = pkv.prefill_workspace(dev())
 
     def store(self):
         pkv.kv_store(self.k_new, self.v_new, self.out_loc, self.k, self.v, dev_status=self.status)
@@ -47,6 +48,7 @@ class Run:
                                      self.x.scale, dev_status=self.status, **kw)
 
     def prefill(self, **kw):
+        kw.setdefault("workspace", self.pws)
         return pkv.paged_prefill_attn(self.q, self.cu, self.k, self.v, self.page_table,
                                       self.seq_lens, self.x.scale, self.x.max_q_len,
                                       dev_status=self.status, **kw)

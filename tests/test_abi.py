@@ -27,7 +27,8 @@ def declared_functions():
 def test_header_declares_the_three_operations():
     names = declared_functions()
     for n in ("pkv_kv_store", "pkv_paged_decode_attn", "pkv_paged_prefill_attn",
-              "pkv_decode_workspace_size", "pkv_status_string", "pkv_version"):
+              "pkv_decode_workspace_size", "pkv_prefill_workspace_size", "pkv_status_string",
+              "pkv_version"):
         assert n in names
 
 
@@ -86,11 +87,13 @@ def test_decode_rejects_bad_arguments(lib):
 
 def _prefill(lib, **kw):
     a = dict(q=FAKE, cu=FAKE, k=FAKE, v=FAKE, pt=FAKE, stride=4, sl=FAKE, B=2, Tq=10, maxq=8,
-             Hq=16, Hkv=8, d=128, ps=16, P=64, scale=0.088, status=NULL, out=FAKE, stream=NULL)
+             Hq=16, Hkv=8, d=128, ps=16, P=64, scale=0.088, ws=FAKE, ws_bytes=256, status=NULL,
+             out=FAKE, stream=NULL)
     a.update(kw)
     return lib.pkv_paged_prefill_attn(a["q"], a["cu"], a["k"], a["v"], a["pt"], a["stride"], a["sl"],
                                       a["B"], a["Tq"], a["maxq"], a["Hq"], a["Hkv"], a["d"], a["ps"],
-                                      a["P"], a["scale"], a["status"], a["out"], a["stream"])
+                                      a["P"], a["scale"], a["ws"], a["ws_bytes"], a["status"], a["out"],
+                                      a["stream"])
 
 
 def test_prefill_rejects_bad_arguments(lib):
@@ -101,7 +104,11 @@ def test_prefill_rejects_bad_arguments(lib):
     assert _prefill(lib, d=256) == U
     assert _prefill(lib, Hq=48, Hkv=8) == U
     assert _prefill(lib, ps=3) == U
+    assert _prefill(lib, ws=NULL) == E              # no workspace
+    assert _prefill(lib, ws_bytes=8) == E           # workspace too small
+    assert _prefill(lib, ws=ctypes.c_void_p(0x10008)) == E   # misaligned workspace
     assert _prefill(lib, Tq=0) == 0
+    assert lib.pkv_prefill_workspace_size() >= 8
 
 
 def test_workspace_size_is_zero_for_bad_sizes(lib):

@@ -75,3 +75,41 @@ def test_prefill_graph_replay():
     torch.cuda.synchronize()
     assert int(status.item()) == 0
     assert max_err(as_f64(out), oracle.run_inputs(x)) <= TOL
+
+
+def test_two_captured_prefill_graphs_replayed_alternately():
+    """Each captured prefill call owns its workspace, so two graphs replayed in
+    turn (or any number of captures) never share queue counters."""
+    xs = [make_inputs(seed=63, Hq=16, Hkv=8, d=128, page_size=16, new_lens=[300, 41, 700],
+                      prefix_lens=[0, 512, 100]),
+          make_inputs(seed=64, Hq=16, Hkv=8, d=128, page_size=16, new_lens=[129, 1000],
+                      prefix_lens=[64, 0])]
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    runs = []
+    for x in xs:
+        k, v = to_dev(x.k_cache), to_dev(x.v_cache)
+        q, kn, vn, loc = to_dev(x.q), to_dev(x.k_new), to_dev(x.v_new), to_dev(x.out_loc)
+        pt, sl, cu = to_dev(x.page_table), to_dev(x.seq_lens), to_dev(x.cu_seqlens_q)
+        out = torch.empty_like(q)
+        pws = pkv.prefill_workspace()
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        with torch.cuda.stream(s):
+            pkv.kv_store(kn, vn, loc, k, v, dev_status=status, stream=s)
+            pkv.paged_prefill_attn(q, cu, k, v, pt, sl, x.scale, x.max_q_len, workspace=pws,
+                                   dev_status=status, out=out, stream=s)
+        s.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            pkv.paged_prefill_attn(q, cu, k, v, pt, sl, x.scale, x.max_q_len, workspace=pws,
+                                   dev_status=status, out=out, stream=s)
+        # the graph holds raw pointers: keep every buffer it uses alive
+        runs.append((x, g, out, status, (k, v, q, kn, vn, loc, pt, sl, cu, pws)))
+    refs = [oracle.run_inputs(x) for x in xs]
+    for rep in range(6):
+        x, g, out, status, _ = runs[rep % 2]
+        out.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        assert max_err(as_f64(out), refs[rep % 2]) <= TOL

@@ -26,3 +26,21 @@ def test_many_calls_of_two_sizes_repeat_bit_for_bit():
             assert big.dev_status() == 0 and small.dev_status() == 0
             assert torch.equal(out_big.view(torch.int16), ref_big.view(torch.int16))
             assert torch.equal(out_small.view(torch.int16), ref_small.view(torch.int16))
+
+
+def test_dirty_workspace_is_reported_and_left_clean():
+    """A workspace whose counters are not zero when a call starts (never
+    cleared, or shared with a call running at the same time) makes that call
+    raise PKV_DEV_BAD_WORKSPACE; the call still returns the counters to zero,
+    so the next call on the same workspace is correct."""
+    r = Run(make_config("ragged_prefill", seed=5)).store()
+    ref = r.prefill()
+    assert r.dev_status() == 0
+    r.pws.view(torch.int32)[0] = 5          # as if 5 queue entries were already taken
+    r.prefill()
+    assert r.dev_status() & pkv.DEV_BAD_WORKSPACE
+    assert int(r.pws.view(torch.int32)[:3].abs().sum().item()) == 0
+    r.status.zero_()
+    out = r.prefill()
+    assert r.dev_status() == 0
+    assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
