@@ -409,6 +409,25 @@ bool encode_q_map(CUtensorMap *map, const void *base, int64_t tokens, int num_q_
 
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// A workspace that the library supplies itself: at most `bytes`, its device
+// address returned by get() (nullptr when that fails).
+struct Scratch {
+    size_t bytes;
+    void *(*get)();
+};
+
+// pkv_paged_decode_attn with `scratch` in place of a caller workspace: every
+// argument and shape check runs first, with the same results as the regular
+// entry point; then sizes whose workspace exceeds scratch.bytes are rejected
+// with PKV_EUNSUPPORTED and scratch.get() supplies the workspace
+// (PKV_ECUDA when it cannot).  Defined in decode.cu.
+pkv_status decode_with_scratch(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf16 *v_cache,
+                               const int32_t *page_table, int64_t page_table_stride,
+                               const int32_t *seq_lens, int batch, int num_q_heads,
+                               int num_kv_heads, int head_dim, int page_size, int64_t num_pages,
+                               float softmax_scale, int32_t *dev_status, pkv_bf16 *out,
+                               void *stream, const Scratch &scratch);
+
 // Launch `kernel` on `stream` as a programmatic dependent of the work before
 // it (see grid_dependency_wait on the device side).
 template <typename... KArgs, typename... Args>

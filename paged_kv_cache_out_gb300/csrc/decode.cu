@@ -758,27 +758,31 @@ extern "C" size_t pkv_decode_workspace_size(int batch, int num_q_heads, int num_
     return prefix + grid * 2 * (static_cast<size_t>(G) * head_dim + 2 * G) * 4;
 }
 
-// Shared argument checks and dispatch of the plain and the fused entry points.
+// Shared argument checks and dispatch of the decode entry points.  With
+// `scratch` set, the workspace arguments are ignored: after every other check
+// has passed, sizes needing more than scratch->bytes are rejected with
+// PKV_EUNSUPPORTED and scratch->get() supplies the workspace.
 static pkv_status decode_entry(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf16 *v_cache,
                                const int32_t *page_table, int64_t page_table_stride,
                                const int32_t *seq_lens, int batch, int num_q_heads,
                                int num_kv_heads, int head_dim, int page_size, int64_t num_pages,
                                float softmax_scale, void *workspace, size_t workspace_bytes,
-                               int32_t *dev_status, pkv_bf16 *out, const Fuse &fz, void *stream) {
+                               int32_t *dev_status, pkv_bf16 *out, const Fuse &fz, void *stream,
+                               const pkv_host::Scratch *scratch) {
     if (batch < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_pages <= 0 ||
         page_table_stride < 0 || page_size <= 0)
         return PKV_EINVAL;
     if (num_q_heads % num_kv_heads != 0) return PKV_EINVAL;
     if (!(softmax_scale == softmax_scale)) return PKV_EINVAL;
     if (batch == 0) return PKV_OK;
-    if (!q || !k_cache || !v_cache || !page_table || !seq_lens || !workspace || !out)
-        return PKV_EINVAL;
+    if (!q || !k_cache || !v_cache || !page_table || !seq_lens || !out) return PKV_EINVAL;
+    if (!scratch && !workspace) return PKV_EINVAL;
     const int G = num_q_heads / num_kv_heads;
     if ((head_dim != 64 && head_dim != 128) || !supported_gqa(G)) return PKV_EUNSUPPORTED;
     if ((page_size & (page_size - 1)) != 0 || page_size > 256) return PKV_EUNSUPPORTED;
     if (batch > kMaxBatch) return PKV_EUNSUPPORTED;
     if (!pkv_host::aligned16(q) || !pkv_host::aligned16(k_cache) || !pkv_host::aligned16(v_cache) ||
-        !pkv_host::aligned16(out) || !pkv_host::aligned16(workspace))
+        !pkv_host::aligned16(out) || (!scratch && !pkv_host::aligned16(workspace)))
         return PKV_EINVAL;
     if (fz.k_new && (!pkv_host::aligned16(fz.k_new) || !pkv_host::aligned16(fz.v_new)))
         return PKV_EINVAL;
@@ -788,8 +792,14 @@ static pkv_status decode_entry(const pkv_bf16 *q, const pkv_bf16 *k_cache, const
     const int64_t max_tiles = (page_table_stride * page_size + T - 1) / T;
     if (static_cast<double>(batch) * num_kv_heads * max_tiles >= 2147483647.0)
         return PKV_EUNSUPPORTED;
-    if (workspace_bytes < pkv_decode_workspace_size(batch, num_q_heads, num_kv_heads, head_dim))
+    const size_t need = pkv_decode_workspace_size(batch, num_q_heads, num_kv_heads, head_dim);
+    if (scratch) {
+        if (need > scratch->bytes) return PKV_EUNSUPPORTED;
+        workspace = scratch->get();
+        if (!workspace) return PKV_ECUDA;
+    } else if (workspace_bytes < need) {
         return PKV_EINVAL;
+    }
     cudaStream_t st = static_cast<cudaStream_t>(stream);
 #define PKV_DECODE_CASE(DD, GG)                                                                 \
     if (head_dim == DD && G == GG)                                                              \
@@ -819,7 +829,7 @@ extern "C" pkv_status pkv_paged_decode_attn(const pkv_bf16 *q, const pkv_bf16 *k
     const Fuse none{nullptr, nullptr, nullptr, nullptr, nullptr};
     return decode_entry(q, k_cache, v_cache, page_table, page_table_stride, seq_lens, batch,
                         num_q_heads, num_kv_heads, head_dim, page_size, num_pages, softmax_scale,
-                        workspace, workspace_bytes, dev_status, out, none, stream);
+                        workspace, workspace_bytes, dev_status, out, none, stream, nullptr);
 }
 
 extern "C" pkv_status pkv_paged_decode_attn_store(
@@ -835,5 +845,18 @@ extern "C" pkv_status pkv_paged_decode_attn_store(
                   reinterpret_cast<__nv_bfloat16 *>(v_cache)};
     return decode_entry(q, k_cache, v_cache, page_table, page_table_stride, seq_lens, batch,
                         num_q_heads, num_kv_heads, head_dim, page_size, num_pages, softmax_scale,
-                        workspace, workspace_bytes, dev_status, out, fz, stream);
+                        workspace, workspace_bytes, dev_status, out, fz, stream, nullptr);
+}
+
+pkv_status pkv_host::decode_with_scratch(const pkv_bf16 *q, const pkv_bf16 *k_cache,
+                                         const pkv_bf16 *v_cache, const int32_t *page_table,
+                                         int64_t page_table_stride, const int32_t *seq_lens,
+                                         int batch, int num_q_heads, int num_kv_heads,
+                                         int head_dim, int page_size, int64_t num_pages,
+                                         float softmax_scale, int32_t *dev_status, pkv_bf16 *out,
+                                         void *stream, const Scratch &scratch) {
+    const Fuse none{nullptr, nullptr, nullptr, nullptr, nullptr};
+    return decode_entry(q, k_cache, v_cache, page_table, page_table_stride, seq_lens, batch,
+                        num_q_heads, num_kv_heads, head_dim, page_size, num_pages, softmax_scale,
+                        nullptr, 0, dev_status, out, none, stream, &scratch);
 }

@@ -38,19 +38,12 @@ extern "C" pkv_status pkv_paged_decode_attn_noalloc(
     const int32_t *page_table, int64_t page_table_stride, const int32_t *seq_lens, int batch,
     int num_q_heads, int num_kv_heads, int head_dim, int page_size, int64_t num_pages,
     float softmax_scale, int32_t *dev_status, pkv_bf16 *out, void *stream) {
-    if (batch == 0) return PKV_OK;
-    const size_t need = pkv_decode_workspace_size(batch, num_q_heads, num_kv_heads, head_dim);
-    if (need > static_cast<size_t>(PKV_NOALLOC_SCRATCH_BYTES)) return PKV_EUNSUPPORTED;
-    void *scratch = nullptr;
-    if (need > 0) {
-        scratch = scratch_for_current_device();
-        if (!scratch) return PKV_ECUDA;
-    }
-    // need == 0 means invalid sizes or no device: the regular entry point
-    // reports which, without launching anything.
-    return pkv_paged_decode_attn(q, k_cache, v_cache, page_table, page_table_stride, seq_lens,
-                                 batch, num_q_heads, num_kv_heads, head_dim, page_size, num_pages,
-                                 softmax_scale, scratch,
-                                 scratch ? static_cast<size_t>(PKV_NOALLOC_SCRATCH_BYTES) : 0,
-                                 dev_status, out, stream);
+    // every argument and shape check runs first, as in pkv_paged_decode_attn;
+    // then sizes beyond the scratch array are rejected and its address looked up
+    static const pkv_host::Scratch scratch{static_cast<size_t>(PKV_NOALLOC_SCRATCH_BYTES),
+                                           &scratch_for_current_device};
+    return pkv_host::decode_with_scratch(q, k_cache, v_cache, page_table, page_table_stride,
+                                         seq_lens, batch, num_q_heads, num_kv_heads, head_dim,
+                                         page_size, num_pages, softmax_scale, dev_status, out,
+                                         stream, scratch);
 }

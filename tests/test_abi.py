@@ -129,3 +129,21 @@ def test_header_is_plain_c99(tmp_path):
     r = subprocess.run([gcc, "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror", "-fsyntax-only",
                         "-I", inc, str(src)], capture_output=True, text=True)
     assert r.returncode == 0, r.stderr
+
+
+def test_noalloc_returns_the_regular_entry_points_status(lib):
+    """The entry point without a workspace runs the same argument checks, in
+    the same order, as pkv_paged_decode_attn (whose workspace here is large
+    enough), so both return the same status for the same bad arguments."""
+    cases = [dict(d=96), dict(Hq=24, Hkv=8), dict(Hq=12, Hkv=8), dict(B=-1), dict(q=NULL),
+             dict(scale=float("nan")), dict(ps=24), dict(B=5000), dict(B=0, P=0), dict(B=0),
+             dict(out=ctypes.c_void_p(0x10002))]
+    for kw in cases:
+        a = dict(q=FAKE, k=FAKE, v=FAKE, pt=FAKE, stride=4, sl=FAKE, B=2, Hq=16, Hkv=8, d=128,
+                 ps=16, P=64, scale=0.088, status=NULL, out=FAKE, stream=NULL)
+        a.update(kw)
+        regular = _decode(lib, **kw)
+        noalloc = lib.pkv_paged_decode_attn_noalloc(
+            a["q"], a["k"], a["v"], a["pt"], a["stride"], a["sl"], a["B"], a["Hq"], a["Hkv"],
+            a["d"], a["ps"], a["P"], a["scale"], a["status"], a["out"], a["stream"])
+        assert noalloc == regular, (kw, noalloc, regular)

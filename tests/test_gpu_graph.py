@@ -113,3 +113,66 @@ def test_two_captured_prefill_graphs_replayed_alternately():
         torch.cuda.synchronize()
         assert int(status.item()) == 0
         assert max_err(as_f64(out), refs[rep % 2]) <= TOL
+
+
+@pytest.mark.parametrize("fused", [False, True])
+def test_padded_replay_at_a_fixed_maximum_batch(fused):
+    """The engines capture decode at a few batch sizes and replay a smaller
+    batch padded to the next captured size with dummy rows (mini-sglang
+    "Engine Class", CUDA Graph Optimization).  Padding rows have seq_len 0
+    and out_loc -1: they produce zero rows and write nothing to the pool."""
+    B_max, B_real = 8, 5
+    x = _decode_inputs(65, [300, 17, 1024, 5, 999], pool_pages=400)
+    Hq, Hkv, d = x.Hq, x.Hkv, x.d
+    pad = B_max - B_real
+
+    def padded(a, fill):
+        a = np.asarray(a)
+        return np.concatenate([a, np.full((pad,) + a.shape[1:], fill, dtype=a.dtype)])
+
+    nan_bits = np.uint16(0x7FC0)
+    q = to_dev(padded(x.q, nan_bits))
+    kn, vn = to_dev(padded(x.k_new, nan_bits)), to_dev(padded(x.v_new, nan_bits))
+    loc = to_dev(padded(x.out_loc, -1))
+    pt = to_dev(padded(x.page_table, -1))
+    sl = to_dev(padded(x.seq_lens, 0))
+    k, v = to_dev(x.k_cache), to_dev(x.v_cache)
+    out = torch.full((B_max, Hq, d), float("nan"), dtype=torch.bfloat16, device="cuda")
+    ws = pkv.decode_workspace(B_max, Hq, Hkv, d)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+
+    def step(stream):
+        if fused:
+            pkv.paged_decode_attn_store(q, kn, vn, loc, k, v, pt, sl, x.scale, workspace=ws,
+                                        dev_status=status, out=out, stream=stream)
+        else:
+            pkv.kv_store(kn, vn, loc, k, v, dev_status=status, stream=stream)
+            pkv.paged_decode_attn(q, k, v, pt, sl, x.scale, workspace=ws, dev_status=status,
+                                  out=out, stream=stream)
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step(s)          # first call outside the capture
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        step(s)
+    # fresh pool, then one replay
+    k.copy_(to_dev(x.k_cache)), v.copy_(to_dev(x.v_cache))
+    out.fill_(float("nan"))
+    torch.cuda.synchronize()
+    g.replay()
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    got = as_f64(out)
+    assert max_err(got[:B_real], oracle.run_inputs(x)) <= TOL
+    assert (got[B_real:] == 0).all()
+    # the pool holds the five new rows at their slots and nothing else changed
+    want_k = x.k_cache.copy().reshape(-1, Hkv, d)
+    want_v = x.v_cache.copy().reshape(-1, Hkv, d)
+    want_k[x.out_loc] = x.k_new
+    want_v[x.out_loc] = x.v_new
+    got_k = k.view(torch.int16).cpu().numpy().view(np.uint16).reshape(-1, Hkv, d)
+    got_v = v.view(torch.int16).cpu().numpy().view(np.uint16).reshape(-1, Hkv, d)
+    assert np.array_equal(got_k, want_k) and np.array_equal(got_v, want_v)

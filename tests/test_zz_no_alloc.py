@@ -5,8 +5,9 @@ memory for a workspace (a runtime that plans all of its memory ahead, a
 plugin that only receives its inputs and outputs): it keeps its scratch in a
 fixed array inside the library.  This file is collected last so that a run
 stopping at the first failure has run every other test before it.  Two calls
-in a row, on different inputs, must each match the regular entry point with a
-caller-provided workspace.
+in a row, on different inputs, must each give bit for bit what the regular
+entry point gives with a caller-provided workspace (the same kernels run on
+the same inputs), and match the oracle.
 """
 import ctypes
 
@@ -14,11 +15,14 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import paged_kv_cache_out_gb300 as pkv
 from synth import make_inputs
-from tests.gpu_util import TOL, Run, as_f64
+from tests.gpu_util import TOL, Run, as_f64, max_err
 
 pytestmark = pytest.mark.gpu
+
+SCRATCH_BYTES = 4194304  # PKV_NOALLOC_SCRATCH_BYTES in include/pkv.h
 
 
 def _call_noalloc(r, out):
@@ -41,22 +45,28 @@ def _inputs(seed):
 
 def test_noalloc_matches_workspace_entry_point_twice():
     for seed in (70, 71):
-        r = Run(_inputs(seed)).store()
+        x = _inputs(seed)
+        r = Run(x).store()
         ref = r.decode()                      # regular entry point, torch-allocated workspace
         out = torch.full_like(ref, float("nan"))
         assert _call_noalloc(r, out) == 0
         assert r.dev_status() == 0
-        got, want = as_f64(out), as_f64(ref)
-        assert np.isfinite(got).all()
-        assert float(np.abs(got - want).max()) <= TOL
+        assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+        assert max_err(as_f64(out), oracle.run_inputs(x)) <= TOL
 
 
-def test_noalloc_rejects_sizes_beyond_its_scratch():
+def test_every_supported_shape_fits_the_scratch_on_this_gpu():
     lib = pkv.load_library()
-    # 16 query heads per KV head at head_dim 128 need more than the fixed scratch
-    need = lib.pkv_decode_workspace_size(4096, 128, 8, 128)
-    assert need > 4194304
-    null = ctypes.c_void_p(0x100)   # never dereferenced: the size check comes first
+    for d in (64, 128):
+        for G in (1, 2, 4, 8):
+            need = lib.pkv_decode_workspace_size(4096, 8 * G, 8, d)  # the largest batch
+            assert 0 < need <= SCRATCH_BYTES, (d, G, need)
+
+
+def test_unsupported_gqa_ratio_is_rejected_without_a_launch():
+    lib = pkv.load_library()
+    null = ctypes.c_void_p(0x100)   # never dereferenced: the shape check comes first
+    # 16 query heads per KV head is not a built shape
     st = lib.pkv_paged_decode_attn_noalloc(null, null, null, null, 64, null, 4096, 128, 8, 128, 16,
                                            1024, 0.1, None, null, None)
     assert st == pkv.binding.EUNSUPPORTED
