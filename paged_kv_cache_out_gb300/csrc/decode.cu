@@ -78,11 +78,22 @@ struct Smem {
 struct Part {
     int64_t W;   // total tiles
     int grid;    // blocks of the main kernel
-    __device__ __forceinline__ int64_t start(int k) const { return (int64_t)k * W / grid; }
+    // floor(k W / grid), as k q + floor(k r / grid) with W = q grid + r: exact,
+    // and k r < grid^2 fits 32 bits
+    __device__ __forceinline__ int64_t start(int k) const {
+        const int64_t q = W / grid;
+        const int r = static_cast<int>(W - q * grid);
+        return (int64_t)k * q + static_cast<int>(static_cast<unsigned>(k * r) / static_cast<unsigned>(grid));
+    }
     __device__ __forceinline__ int block_of(int64_t x) const {
         return static_cast<int>(((x + 1) * grid - 1) / W);
     }
 };
+
+// Floats of one partial state in the workspace: G x D weighted sums, then a
+// (max, sum) pair per head, padded to a multiple of 4 so that every state
+// starts on a 16-byte boundary (the merge kernel reads it as float4).
+__host__ __device__ constexpr int part_stride(int G, int D) { return ((G * D + 2 * G + 3) / 4) * 4; }
 
 __device__ __forceinline__ int ntiles_of(int L, int64_t cap, int T) {
     return (L > 0 && L <= cap) ? (L + T - 1) / T : 0;
@@ -587,7 +598,7 @@ __global__ void __launch_bounds__(kThreads, G <= 4 ? kCtasPerSm : 1)
                 const float v = bad_piece ? __int_as_float(0x7fc00000) : acc / sum;
                 out[((int64_t)p.b * Hq + (int64_t)p.g * G) * D + idx] = __float2bfloat16_rn(v);
             } else {
-                float *part_o = ws_part + (int64_t)slot * (G * D + 2 * G);
+                float *part_o = ws_part + (int64_t)slot * part_stride(G, D);
                 part_o[idx] = acc;
                 if (idx % D == 0) {
                     part_o[G * D + 2 * h] = bad_piece ? __int_as_float(0x7fc00000) : mx;
@@ -602,13 +613,22 @@ __global__ void __launch_bounds__(kThreads, G <= 4 ? kCtasPerSm : 1)
 
 // Merge of the partial states of segments that were cut across blocks, and
 // the output of segments with no keys (zeros, or NaN for an invalid length).
+// One block per segment; thread (v, kl) owns the 4 output values of float4 v
+// and the partial states k0 + kl, k0 + kl + KL, ... of the segment, so all of
+// a thread's loads are independent and the KL partial sums of a vector meet
+// in warp shuffles.
+constexpr int kMergeThreads = 256;
 template <int D, int G>
-__global__ void __launch_bounds__(128)
+__global__ void __launch_bounds__(kMergeThreads)
     decode_merge_kernel(const int32_t *__restrict__ seq_lens, const int32_t *__restrict__ ws_prefix,
                         const float *__restrict__ ws_part, int B, int Hkv, int64_t cap, int grid,
                         int32_t *dev_status, __nv_bfloat16 *__restrict__ out, const Fuse fz,
                         int64_t num_slots) {
-    using S = Shape<D, G>;
+    constexpr int E = G * D;                       // output values of a segment
+    constexpr int NV = E / 4;                      // float4 pieces
+    constexpr int KL = kMergeThreads / NV;         // partial states per piece in parallel
+    static_assert(KL >= 1 && KL <= 32 && (KL & (KL - 1)) == 0, "merge layout");
+    constexpr int STRIDE = part_stride(G, D);      // floats per partial state
     grid_dependency_wait();  // partial states come from the main kernel
     const int b = blockIdx.x / Hkv, g = blockIdx.x % Hkv;
     const int Hq = Hkv * G;
@@ -626,7 +646,7 @@ __global__ void __launch_bounds__(128)
                 atomicOr(dev_status, PKV_DEV_BAD_SLOT);
         }
         if (bad && g == 0 && threadIdx.x == 0 && dev_status) atomicOr(dev_status, PKV_DEV_BAD_SEQLEN);
-        for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x)
+        for (int idx = threadIdx.x; idx < E; idx += blockDim.x)
             orow[idx] = __float2bfloat16_rn(bad ? __int_as_float(0x7fc00000) : 0.f);
         return;
     }
@@ -635,30 +655,57 @@ __global__ void __launch_bounds__(128)
     const int64_t s1 = s0 + nt;
     const int k0 = part.block_of(s0), k1 = part.block_of(s1 - 1);
     if (k0 == k1) return;  // written directly by the main kernel
-    (void)S::T;
-    // Blocks k0 < k <= k1 whose range is empty (fewer tiles than blocks) hold
-    // no partial state of this segment and are skipped.
-    for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
-        const int h = idx / D;
-        float mx = kNegBig;
-        bool bad = false;
-        for (int k = k0; k <= k1; ++k) {
-            if (part.start(k + 1) <= part.start(k)) continue;
-            const int slot = 2 * k + ((k == k0 && s0 != part.start(k0)) ? 1 : 0);
-            const float mk = ws_part[(int64_t)slot * (G * D + 2 * G) + G * D + 2 * h];
-            bad |= isnan(mk);
-            mx = fmaxf(mx, mk);
-        }
-        float sum = 0.f, acc = 0.f;
-        for (int k = k0; k <= k1; ++k) {
-            if (part.start(k + 1) <= part.start(k)) continue;
-            const int slot = 2 * k + ((k == k0 && s0 != part.start(k0)) ? 1 : 0);
-            const float *pk = ws_part + (int64_t)slot * (G * D + 2 * G);
-            const float w = ex2(pk[G * D + 2 * h] - mx);
-            sum = fmaf(pk[G * D + 2 * h + 1], w, sum);
-            acc = fmaf(pk[idx], w, acc);
-        }
-        orow[idx] = __float2bfloat16_rn(bad ? __int_as_float(0x7fc00000) : acc / sum);
+    const int v = threadIdx.x / KL, kl = threadIdx.x % KL;
+    const int h = (4 * v) / D;  // query head of this piece
+    // the partial-state slot of block k, or -1 for blocks whose range is empty
+    // (fewer tiles than blocks): they hold no state of this segment
+    auto slot_of = [&](int k) -> int {
+        const int64_t a = part.start(k), z = part.start(k + 1);
+        if (z <= a) return -1;
+        return 2 * k + ((k == k0 && s0 != a) ? 1 : 0);
+    };
+    float mx = kNegBig;
+    bool bad = false;
+    for (int k = k0 + kl; k <= k1; k += KL) {
+        const int sl = slot_of(k);
+        if (sl < 0) continue;
+        const float mk = ws_part[(int64_t)sl * STRIDE + E + 2 * h];
+        bad |= isnan(mk);
+        mx = fmaxf(mx, mk);
+    }
+#pragma unroll
+    for (int o = KL / 2; o >= 1; o >>= 1) {
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        bad |= __shfl_xor_sync(0xffffffffu, bad ? 1 : 0, o) != 0;
+    }
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float sum = 0.f;
+    for (int k = k0 + kl; k <= k1; k += KL) {
+        const int sl = slot_of(k);
+        if (sl < 0) continue;
+        const float *pk = ws_part + (int64_t)sl * STRIDE;
+        const float w = ex2(pk[E + 2 * h] - mx);
+        sum = fmaf(pk[E + 2 * h + 1], w, sum);
+        const float4 o4 = *reinterpret_cast<const float4 *>(pk + 4 * v);
+        acc.x = fmaf(o4.x, w, acc.x);
+        acc.y = fmaf(o4.y, w, acc.y);
+        acc.z = fmaf(o4.z, w, acc.z);
+        acc.w = fmaf(o4.w, w, acc.w);
+    }
+#pragma unroll
+    for (int o = KL / 2; o >= 1; o >>= 1) {
+        sum += __shfl_xor_sync(0xffffffffu, sum, o);
+        acc.x += __shfl_xor_sync(0xffffffffu, acc.x, o);
+        acc.y += __shfl_xor_sync(0xffffffffu, acc.y, o);
+        acc.z += __shfl_xor_sync(0xffffffffu, acc.z, o);
+        acc.w += __shfl_xor_sync(0xffffffffu, acc.w, o);
+    }
+    if (kl == 0) {
+        const float inv = 1.f / sum;
+        const float nan = __int_as_float(0x7fc00000);
+        const uint32_t lo = pack_bf16x2(bad ? nan : acc.x * inv, bad ? nan : acc.y * inv);
+        const uint32_t hi = pack_bf16x2(bad ? nan : acc.z * inv, bad ? nan : acc.w * inv);
+        *reinterpret_cast<uint2 *>(orow + 4 * v) = make_uint2(lo, hi);
     }
 }
 
@@ -729,7 +776,7 @@ static pkv_status launch(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_b
                                    ws_part, ws_prefix, dev_status,
                                    reinterpret_cast<__nv_bfloat16 *>(out), fz) != cudaSuccess)
         return PKV_ECUDA;
-    if (pkv_host::launch_dependent(decode_merge_kernel<D, G>, dim3(B * Hkv), dim3(128), 0, stream,
+    if (pkv_host::launch_dependent(decode_merge_kernel<D, G>, dim3(B * Hkv), dim3(kMergeThreads), 0, stream,
                                    seq_lens, static_cast<const int32_t *>(ws_prefix),
                                    static_cast<const float *>(ws_part), B, Hkv,
                                    pt_stride * page_size, grid, dev_status,
@@ -755,7 +802,7 @@ extern "C" size_t pkv_decode_workspace_size(int batch, int num_q_heads, int num_
     const int G = num_q_heads / num_kv_heads;
     const size_t grid = static_cast<size_t>(dev.sm_count) * kCtasPerSm;
     const size_t prefix = ((static_cast<size_t>(batch) + 1) * 4 + 255) & ~size_t(255);
-    return prefix + grid * 2 * (static_cast<size_t>(G) * head_dim + 2 * G) * 4;
+    return prefix + grid * 2 * static_cast<size_t>(part_stride(G, head_dim)) * 4;
 }
 
 // Shared argument checks and dispatch of the decode entry points.  With
