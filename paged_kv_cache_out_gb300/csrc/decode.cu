@@ -99,6 +99,15 @@ __device__ __forceinline__ int ntiles_of(int L, int64_t cap, int T) {
     return (L > 0 && L <= cap) ? (L + T - 1) / T : 0;
 }
 
+// Work units of a segment in the balanced partition: its tiles plus kLead
+// units standing for the fixed cost of a segment piece (the page-id read, the
+// q copy, the reduction across row groups and the output write), so that a
+// block whose range holds many short segments gets fewer tiles.  A segment
+// occupies [kLead lead units][its tiles]; lead units load nothing.  Empty
+// segments occupy no units.
+constexpr int kLead = 2;
+__device__ __forceinline__ int units_of(int ntiles) { return ntiles > 0 ? ntiles + kLead : 0; }
+
 // Largest b in [0, B) with prefix[b] <= x (x < prefix[B]).
 __device__ __forceinline__ int owner_search(const int32_t *prefix, int B, int64_t x) {
     int lo = 0, hi = B;
@@ -111,32 +120,35 @@ __device__ __forceinline__ int owner_search(const int32_t *prefix, int B, int64_
 
 struct Piece {
     int b, g;
-    int t0, t1;         // tile range inside the segment
+    int t0, t1;         // tile range inside the segment (t1 <= t0: lead units only)
     int nt;             // tiles of the whole segment
-    bool whole;         // covers the whole segment
+    bool whole;         // covers all tiles of the segment
     bool block_first;   // first piece of this block
 };
 
+// The next piece of the block's unit range, with its units turned into tiles.
 __device__ __forceinline__ bool next_piece(int64_t &pos, int64_t end, int64_t block_start,
                                            const int32_t *prefix, int B, int Hkv, Piece &p) {
     if (pos >= end) return false;
     const int b = owner_search(prefix, B, pos);
-    const int nt = (prefix[b + 1] - prefix[b]) / Hkv;
+    const int nu = (prefix[b + 1] - prefix[b]) / Hkv;  // units of each segment of b
     const int64_t rel = pos - prefix[b];
     p.b = b;
-    p.g = static_cast<int>(rel / nt);
-    p.t0 = static_cast<int>(rel % nt);
-    const int64_t seg_end = prefix[b] + (int64_t)(p.g + 1) * nt;
+    p.g = static_cast<int>(rel / nu);
+    const int u0 = static_cast<int>(rel % nu);
+    const int64_t seg_end = prefix[b] + (int64_t)(p.g + 1) * nu;
     const int64_t pend = end < seg_end ? end : seg_end;
-    p.t1 = p.t0 + static_cast<int>(pend - pos);
-    p.nt = nt;
-    p.whole = (p.t0 == 0) && (pend == seg_end);
+    const int u1 = u0 + static_cast<int>(pend - pos);
+    p.t0 = u0 > kLead ? u0 - kLead : 0;
+    p.t1 = u1 - kLead;
+    p.nt = nu - kLead;
+    p.whole = (u0 <= kLead) && (pend == seg_end);
     p.block_first = (pos == block_start);
     pos = pend;
     return true;
 }
 
-// Block-wide exclusive scan: prefix[b] = Hkv * sum_{b' < b} ntiles(b'); the
+// Block-wide exclusive scan: prefix[b] = Hkv * sum_{b' < b} units(b'); the
 // lengths themselves are kept in lens[b].
 __device__ void build_prefix(int32_t *prefix, int32_t *lens, const int32_t *seq_lens, int B,
                              int Hkv, int64_t cap, int T,
@@ -149,7 +161,7 @@ __device__ void build_prefix(int32_t *prefix, int32_t *lens, const int32_t *seq_
     for (int b = lo; b < hi; ++b) {
         const int L = seq_lens[b];
         lens[b] = L;
-        local += ntiles_of(L, cap, T) * Hkv;
+        local += units_of(ntiles_of(L, cap, T)) * Hkv;
     }
     // inclusive scan of `local` over the block
     const int lane = tid & 31, warp = tid >> 5;
@@ -174,7 +186,7 @@ __device__ void build_prefix(int32_t *prefix, int32_t *lens, const int32_t *seq_
     int run = scratch[warp] + v - local;  // exclusive prefix of this thread's chunk
     for (int b = lo; b < hi; ++b) {
         prefix[b] = run;
-        run += ntiles_of(lens[b], cap, T) * Hkv;
+        run += units_of(ntiles_of(lens[b], cap, T)) * Hkv;
     }
     if (tid == 0) prefix[B] = scratch[kThreads / 32];
     __syncthreads();
@@ -225,9 +237,9 @@ __device__ void store_block_rows(const Fuse &fz, const int32_t *prefix, const in
     bool flag = false;
     for (int64_t o = o0 + ctid; o <= o1; o += kConsumerWarps * 32) {
         const int b = static_cast<int>(o / Hkv), g = static_cast<int>(o % Hkv);
-        const int nt = (prefix[b + 1] - prefix[b]) / Hkv;
-        if (nt == 0) continue;  // no keys: the merge kernel stores its row
-        const int64_t last = prefix[b] + (int64_t)(g + 1) * nt - 1;
+        const int nu = (prefix[b + 1] - prefix[b]) / Hkv;
+        if (nu == 0) continue;  // no keys: the merge kernel stores its row
+        const int64_t last = prefix[b] + (int64_t)(g + 1) * nu - 1;  // its last tile
         if (last < t0 || last >= t1) continue;
         const int64_t slot = fz.out_loc[b];
         if (slot < 0) continue;
@@ -328,6 +340,7 @@ __global__ void __launch_bounds__(kThreads, G <= 4 ? kCtasPerSm : 1)
         // of 32 boxes, the next window loaded one window ahead
         const int bpt = T / box_rows;
         while (ok && next_piece(pos, my_end, my_start, prefix, B, Hkv, p)) {
+            if (p.t1 <= p.t0) continue;  // lead units only: nothing to load
             const int L = lens[p.b];
             const int32_t *prow = page_table + (int64_t)p.b * pt_stride;
             auto load_window = [&](int w) -> int {
@@ -439,6 +452,7 @@ __global__ void __launch_bounds__(kThreads, G <= 4 ? kCtasPerSm : 1)
     uint32_t it = 0;
     bool ok = true;
     while (ok && next_piece(pos, my_end, my_start, prefix, B, Hkv, p)) {
+        if (p.t1 <= p.t0) continue;  // lead units only: nothing to do
         const int L = lens[p.b];
 #pragma unroll
         for (int h = 0; h < G; ++h) {
@@ -633,8 +647,8 @@ __global__ void __launch_bounds__(kMergeThreads)
     const int b = blockIdx.x / Hkv, g = blockIdx.x % Hkv;
     const int Hq = Hkv * G;
     __nv_bfloat16 *orow = out + ((int64_t)b * Hq + (int64_t)g * G) * D;
-    const int nt = (ws_prefix[b + 1] - ws_prefix[b]) / Hkv;
-    if (nt == 0) {
+    const int nu = (ws_prefix[b + 1] - ws_prefix[b]) / Hkv;  // units of the segment
+    if (nu == 0) {
         const int L = seq_lens[b];
         const bool bad = (L < 0 || L > cap);
         // fused store of a sequence that attends to nothing: still store its row
@@ -651,18 +665,21 @@ __global__ void __launch_bounds__(kMergeThreads)
         return;
     }
     Part part{ws_prefix[B], grid};
-    const int64_t s0 = ws_prefix[b] + (int64_t)g * nt;
-    const int64_t s1 = s0 + nt;
-    const int k0 = part.block_of(s0), k1 = part.block_of(s1 - 1);
+    const int64_t s0 = ws_prefix[b] + (int64_t)g * nu;  // the segment's units, lead units first
+    const int64_t s1 = s0 + nu;
+    // blocks holding its tiles (blocks before k0 hold lead units only)
+    const int k0 = part.block_of(s0 + kLead), k1 = part.block_of(s1 - 1);
     if (k0 == k1) return;  // written directly by the main kernel
     const int v = threadIdx.x / KL, kl = threadIdx.x % KL;
     const int h = (4 * v) / D;  // query head of this piece
     // the partial-state slot of block k, or -1 for blocks whose range is empty
-    // (fewer tiles than blocks): they hold no state of this segment
+    // (fewer units than blocks): they hold no state of this segment.  The
+    // segment's piece is the block's first piece (slot 2k) unless the segment
+    // starts after the block's range does (slot 2k + 1: its last piece).
     auto slot_of = [&](int k) -> int {
         const int64_t a = part.start(k), z = part.start(k + 1);
         if (z <= a) return -1;
-        return 2 * k + ((k == k0 && s0 != a) ? 1 : 0);
+        return 2 * k + ((k == k0 && s0 > a) ? 1 : 0);
     };
     float mx = kNegBig;
     bool bad = false;
@@ -836,7 +853,7 @@ static pkv_status decode_entry(const pkv_bf16 *q, const pkv_bf16 *k_cache, const
     if (num_pages * page_size > 0x7fffffffll) return PKV_EUNSUPPORTED;
     // total tiles must fit the block's int32 prefix sums
     const int T = head_dim == 128 ? Shape<128, 1>::T : Shape<64, 1>::T;  // T depends on head_dim only
-    const int64_t max_tiles = (page_table_stride * page_size + T - 1) / T;
+    const int64_t max_tiles = (page_table_stride * page_size + T - 1) / T + kLead;  // units
     if (static_cast<double>(batch) * num_kv_heads * max_tiles >= 2147483647.0)
         return PKV_EUNSUPPORTED;
     const size_t need = pkv_decode_workspace_size(batch, num_q_heads, num_kv_heads, head_dim);
