@@ -78,12 +78,18 @@ constexpr float kRescaleLog2 = 8.0f;  // lazy rescale threshold (factor 256)
 constexpr uint32_t kTmemCols = 512;
 // Registers per thread: the block launches with kRegsLaunch for all 384
 // threads; then warpgroup 2 (producer, MMA issuer, loaders) gives up all but
-// kRegsLow and the two softmax warpgroups take kRegsHigh each, so that a row's
-// 128 scores and the softmax's temporaries fit without spilling.
-// 256 x kRegsHigh + 128 x kRegsLow must not exceed 384 x kRegsLaunch.
-constexpr int kRegsLaunch = 168, kRegsHigh = 208, kRegsLow = 88;
-static_assert(8 * 32 * kRegsHigh + 4 * 32 * kRegsLow <= kThreads * kRegsLaunch,
-              "register split exceeds the block's registers");
+// regs_low and the two softmax warpgroups take regs_high each, so that a row's
+// 128 scores and the softmax's temporaries fit without spilling.  Pages of
+// fewer than 8 tokens are gathered by the loaders with per-key copies, which
+// need more of their registers.  256 x regs_high + 128 x regs_low must not
+// exceed 384 x kRegsLaunch.
+constexpr int kRegsLaunch = 168;
+template <bool SMALL>
+struct RegSplit {
+    static constexpr int high = SMALL ? 192 : 208, low = SMALL ? 120 : 88;
+    static_assert(8 * 32 * high + 4 * 32 * low <= kThreads * kRegsLaunch,
+                  "register split exceeds the block's registers");
+};
 
 template <int D>
 struct Layout {
@@ -179,7 +185,9 @@ __device__ __forceinline__ int group_weight(int grp, int B, int mtiles, int64_t 
     return (L - n + min(n, t0 + NQ * TOK) + BN - 1) / BN;
 }
 
-template <int D, int G>
+// SMALL: pages of fewer than 8 tokens (gathered key by key); otherwise every
+// page of a tile comes in as TMA boxes.
+template <int D, int G, bool SMALL>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                    const __grid_constant__ CUtensorMap vmap, const __nv_bfloat16 *__restrict__ k_cache,
@@ -295,7 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t sV = smem_u32(smem + Lo::OFF_V);
 
     if (warp >= kProducerWarp) {
-    regs_decrease<kRegsLow>();
+    regs_decrease<RegSplit<SMALL>::low>();
     if (warp != kMmaWarp) {
         // ================================================================ producer and loaders
         // Warp 8 takes the items and publishes them, and loads the Q tiles;
@@ -308,18 +316,42 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t pol_q = l2_evict_first_policy();
         if (lane == 0) {
             if (li == 0) prefetch_tmap(&qmap);
-            if (box_rows >= 8) {
+            if (!SMALL) {
                 prefetch_tmap(&kmap);
                 prefetch_tmap(&vmap);
             }
         }
         const int ps_mask = (1 << ps_log2) - 1;
-        const int bpt = box_rows >= 8 ? BN / box_rows : 1;  // page boxes per tile (<= 16)
+        const int bpt = !SMALL ? BN / box_rows : 1;  // page boxes per tile (<= 16)
         constexpr int NBLK = D / 64;                        // 64-column blocks of a row
         uint32_t kt = 0, vt = 0;  // K and V tiles loaded so far (ring position)
         bool ok = true;
         bool first = true;        // the first item of a block is its block index
         Item itm;
+        // small pages: the full barrier of this warp's last gathered tile, whose
+        // copies may still be in flight (0: none).  flush_gather waits for them
+        // (all but the newest group when keep_one), makes them visible to the
+        // tensor core and arrives on that barrier.
+        uint32_t gather_pending = 0;
+        // small pages: the key rows a loader lane copies, KPI keys per warp
+        // instruction, instructions li, li + 3, ... of a tile
+        constexpr int CHK = D / 8;                // 16-byte pieces of a row
+        constexpr int KPI = 32 / CHK;             // keys per warp instruction
+        constexpr int NGRP = BN / KPI;            // instructions per tile
+        constexpr int NIT = (NGRP + kLoaders - 1) / kLoaders;
+        static_assert(BN == 128, "the page ids of a tile's keys are held 4 per lane");
+        int gpg[4], gpg_next[4];  // page ids of keys lane + 32 r of this tile / the next tile
+        auto flush_gather = [&](bool keep_one) {
+            if (!gather_pending) return;
+            if (keep_one)
+                cp_async_wait<1>();
+            else
+                cp_async_wait<0>();
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(gather_pending);
+            gather_pending = 0;
+        };
         for (uint32_t ii = 0; ok; ++ii) {
             const int slot = ii % kItemSlots;
             int p = -1;
@@ -378,10 +410,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 
             const int32_t *prow = page_table + (int64_t)itm.r * pt_stride;
             const int L = itm.L, g = itm.g;
+            auto load_ids = [&](int j, int *dstp) {
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    const int kk = j * BN + r * 32 + lane;
+                    dstp[r] = kk < L ? prow[kk >> ps_log2] : 0;
+                }
+            };
             // page ids in warp-wide windows of 32 page boxes, the next window loaded ahead
             auto load_window = [&](int w) -> int {
                 const int key = (32 * w + lane) * box_rows;
-                return (box_rows >= 8 && key < L) ? prow[key >> ps_log2] : 0;
+                return (!SMALL && key < L) ? prow[key >> ps_log2] : 0;
             };
             int w_cur = 0;
             int pg_cur = load_window(0), pg_nxt = load_window(1);
@@ -409,7 +448,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int nkeys = min(BN, L - key0);  // keys of this tile that exist in pages
                 if (t >= static_cast<uint32_t>(ns) && !mbar_wait_warp(empty, ph ^ 1, abort_flag, dev_status))
                     return false;
-                if (box_rows >= 8) {
+                if constexpr (!SMALL) {
                     const int nbox = (nkeys + box_rows - 1) / box_rows;  // page boxes, <= 16
                     const int b = li + kLoaders * lane;                  // this lane's box
                     const int pb = b / NBLK, blk = b % NBLK;
@@ -434,30 +473,48 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     __syncwarp();
                 } else {
-                    // small pages: gather 16-byte chunks, swizzle, zero rows past the sequence
+                    // small pages: every key's row gathered with 16-byte copies
+                    // straight into the swizzled layout (keys past the sequence or
+                    // on a page outside the pool are zero-filled).  The copies of
+                    // a tile complete while the warp issues its next tile; then
+                    // the warp waits for them, orders them before the tensor
+                    // core's reads and arrives (see flush_gather).
                     const __nv_bfloat16 *base = kv ? v_cache : k_cache;
-                    bool bad = false;
-                    for (int idx = li * 32 + lane; idx < BN * (D / 8); idx += kLoaders * 32) {
-                        const int key = idx / (D / 8), ch = idx % (D / 8);
-                        uint4 val = make_uint4(0u, 0u, 0u, 0u);
-                        if (key < nkeys) {
-                            const int kk = key0 + key;
-                            const int pg = prow[kk >> ps_log2];
-                            if (pg >= 0 && pg < num_pages) {
-                                const int64_t sl = ((int64_t)pg << ps_log2) + (kk & ps_mask);
-                                val = __ldg(reinterpret_cast<const uint4 *>(base + (sl * Hkv + g) * D +
-                                                                            ch * 8));
-                            } else {
-                                bad = true;
-                            }
+                    // page ids of this tile's keys: loaded for K(j) (or
+                    // prefetched while V(j-1) was issued) and reused for V(j),
+                    // which prefetches those of tile j + 1
+                    if (kv == 0) {
+                        if (j == 0) {
+                            load_ids(0, gpg);
+                        } else {
+#pragma unroll
+                            for (int r = 0; r < 4; ++r) gpg[r] = gpg_next[r];
                         }
-                        *reinterpret_cast<uint4 *>(smem + (dst - smem_u32(smem)) +
-                                                   swz_offset(key, ch, BN)) = val;
+                    } else if (j + 1 < itm.n_kt) {
+                        load_ids(j + 1, gpg_next);
                     }
+                    bool bad = false;
+#pragma unroll
+                    for (int it = 0; it < NIT; ++it) {
+                        const int m = li + kLoaders * it;
+                        if (m >= NGRP) break;
+                        const int key = m * KPI + lane / CHK, ch = lane % CHK;
+                        const int kk = key0 + key;
+                        // the instruction's keys lie in one 32-key block (warp-uniform)
+                        const int blk32 = (m * KPI) >> 5;
+                        const int held = blk32 == 0 ? gpg[0] : blk32 == 1 ? gpg[1] : blk32 == 2 ? gpg[2] : gpg[3];
+                        const int pg = __shfl_sync(0xffffffffu, held, key & 31);
+                        const bool in_seq = key < nkeys;
+                        const bool ok_page = in_seq && pg >= 0 && pg < num_pages;
+                        bad |= in_seq && !ok_page;
+                        const int64_t sl = ok_page ? ((int64_t)pg << ps_log2) + (kk & ps_mask) : 0;
+                        cp_async16(dst + swz_offset(key, ch, BN), base + (sl * Hkv + g) * D + ch * 8,
+                                   ok_page ? 16u : 0u);
+                    }
+                    cp_async_commit();
                     if (__any_sync(0xffffffffu, bad) && lane == 0) bad_flag[slot] = 1;
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(full);
+                    flush_gather(true);
+                    gather_pending = full;
                 }
                 return true;
             };
@@ -487,7 +544,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int blk = 0; blk < NBLK; ++blk)
                             tma_prefetch_3d(&qmap, blk * 64, g * G, itm.cu0 + itm.tbeg[qt]);
                 }
-                if (box_rows >= 8) {
+                if (!SMALL) {
                     const int nbox0 = (min(BN, L) + box_rows - 1) / box_rows;
                     const int pg0 = page_of(0, lane);
                     if (lane < nbox0 && pg0 >= 0 && pg0 < num_pages) {
@@ -512,6 +569,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ok = load_tile(1, j, vt + j);
                 if (ok && j + 1 < itm.n_kt) ok = load_tile(0, j + 1, kt + j + 1);
             }
+            flush_gather(false);  // the item's last gathered tile is needed now
             kt += itm.n_kt;
             vt += itm.n_kt;
             if (ok && li > 0) {
@@ -519,6 +577,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0) mbar_arrive(BAR(B_IEMPTY(slot)));
             }
         }
+
     } else if (warp == kMmaWarp) {
         // ================================================================ MMA issuer
         // One lane issues the MMAs of both query tiles in a fixed order, so a
@@ -649,7 +708,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     } else {
         // ================================================================ softmax
-        regs_increase<kRegsHigh>();
+        regs_increase<RegSplit<SMALL>::high>();
         const int qt = warp >> 2;                  // query tile of this warpgroup
         const int row = tid & 127;                 // TMEM lane == tile row
         const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
@@ -828,7 +887,9 @@ static bool prepare(const pkv_host::DeviceInfo &dev) {
     std::lock_guard<std::mutex> lk(mu);
     if (!ready[dev.device]) {
         if (Layout<D>::bytes() > static_cast<size_t>(dev.max_smem_optin)) return false;
-        if (cudaFuncSetAttribute(prefill_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(prefill_kernel<D, G, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(Layout<D>::bytes())) != cudaSuccess ||
+            cudaFuncSetAttribute(prefill_kernel<D, G, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(Layout<D>::bytes())) != cudaSuccess)
             return false;
         ready[dev.device] = true;
@@ -867,7 +928,8 @@ static pkv_status launch(const pkv_bf16 *q, const int32_t *cu, const pkv_bf16 *k
     if (items > 0x7fffffffll) return PKV_EUNSUPPORTED;
     // persistent: one block per SM (fewer when there are fewer items)
     const int grid = items < dev.sm_count ? static_cast<int>(items) : dev.sm_count;
-    prefill_kernel<D, G><<<static_cast<unsigned>(grid), kThreads, Layout<D>::bytes(), stream>>>(
+    auto kernel = box_rows >= 8 ? prefill_kernel<D, G, false> : prefill_kernel<D, G, true>;
+    kernel<<<static_cast<unsigned>(grid), kThreads, Layout<D>::bytes(), stream>>>(
         qmap, kmap, vmap, reinterpret_cast<const __nv_bfloat16 *>(k_cache),
         reinterpret_cast<const __nv_bfloat16 *>(v_cache), cu, page_table, pt_stride, seq_lens, B, Tq,
         max_q_len, Hkv, ps_log2, box_rows, num_pages, scale * kLog2e, mtiles, sched, dev_status,
