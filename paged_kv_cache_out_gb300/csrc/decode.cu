@@ -275,6 +275,7 @@ __device__ void store_block_rows(const Fuse &fz, const int32_t *prefix, const in
 template <int D, int G, bool FUSE>
 __global__ void __launch_bounds__(kThreads, G <= 4 ? kCtasPerSm : 1)
     decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                  const __nv_bfloat16 *__restrict__ k_cache, const __nv_bfloat16 *__restrict__ v_cache,
                   const __nv_bfloat16 *__restrict__ q, const int32_t *__restrict__ page_table,
                   int64_t pt_stride, const int32_t *__restrict__ seq_lens, int B, int Hkv,
                   int ps_log2, int box_rows, int64_t num_pages, float scale_log2,
@@ -303,8 +304,11 @@ __global__ void __launch_bounds__(kThreads, G <= 4 ? kCtasPerSm : 1)
     grid_dependency_wait();  // the pool rows of this step are written by the kernel before
     allow_dependents();      // the merge kernel may become resident and wait for us
     if (tid == 0) {
+        // full: the producer's arrival with the tx bytes; for pages of fewer
+        // than 8 tokens also one arrival per producer lane when its copies land
+        const uint32_t full_count = box_rows < 8 ? 33u : 1u;
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(smem_u32(&bars[s]), 1);                        // full: producer + tx bytes
+            mbar_init(smem_u32(&bars[s]), full_count);
             mbar_init(smem_u32(&bars[STAGES + s]), kConsumerWarps);  // empty: one per consumer warp
         }
         mbar_init(smem_u32(&bars[2 * STAGES]), kConsumerWarps);  // fused stores written
@@ -331,6 +335,7 @@ __global__ void __launch_bounds__(kThreads, G <= 4 ? kCtasPerSm : 1)
         }
         const int ps_mask = (1 << ps_log2) - 1;
         const uint32_t box_bytes = static_cast<uint32_t>(box_rows) * D * 2;
+        const bool small = box_rows < 8;  // gather key rows instead of page boxes
         int64_t pos = my_start;
         Piece p;
         uint32_t it = 0;
@@ -363,30 +368,6 @@ __global__ void __launch_bounds__(kThreads, G <= 4 ? kCtasPerSm : 1)
                 }
                 const int tok0 = tile * T;
                 const int ntok = min(T, L - tok0);
-                const int nbox = (ntok + box_rows - 1) / box_rows;
-                // page ids of this tile's boxes (at most T boxes: two per lane)
-                int pg[2] = {0, 0};
-                bool bad = false;
-                if (bpt <= 32) {
-                    const int b0 = tile * bpt;
-                    if ((b0 >> 5) != w_cur) {
-                        w_cur = b0 >> 5;
-                        pg_cur = pg_nxt;
-                        pg_nxt = load_window(w_cur + 1);
-                    }
-                    pg[0] = __shfl_sync(0xffffffffu, pg_cur, (b0 + (lane % bpt)) & 31);
-                    if (lane < nbox && (pg[0] < 0 || pg[0] >= num_pages)) bad = true;
-                } else {
-#pragma unroll
-                    for (int k = 0; k < 2; ++k) {
-                        const int i = lane + 32 * k;
-                        if (i < nbox) {
-                            pg[k] = prow[(tok0 + i * box_rows) >> ps_log2];
-                            if (pg[k] < 0 || pg[k] >= num_pages) bad = true;
-                        }
-                    }
-                }
-                bad = __any_sync(0xffffffffu, bad);
                 const bool first = (tile == p.t0);
                 // fused store: the consumers write the new rows of the block's
                 // segments first; a segment's last tile (which holds its new
@@ -398,28 +379,98 @@ __global__ void __launch_bounds__(kThreads, G <= 4 ? kCtasPerSm : 1)
                     }
                     stores_seen = true;
                 }
-                const uint32_t bytes = (bad ? 0u : 2u * box_bytes * nbox) +
-                                       (first ? static_cast<uint32_t>(G * D * 2) : 0u);
                 uint8_t *st = ring + s * M::STAGE_BYTES;
                 const uint32_t full = smem_u32(&bars[s]);
-                if (lane == 0) {
-                    flags[s] = bad ? 1 : 0;
-                    mbar_arrive_expect_tx(full, bytes);
-                }
-                __syncwarp();
-                if (!bad) {
+                const uint32_t q_bytes = first ? static_cast<uint32_t>(G * D * 2) : 0u;
+                if (!small) {
+                    const int nbox = (ntok + box_rows - 1) / box_rows;
+                    // page ids of this tile's boxes (at most T boxes: two per lane)
+                    int pg[2] = {0, 0};
+                    bool bad = false;
+                    if (bpt <= 32) {
+                        const int b0 = tile * bpt;
+                        if ((b0 >> 5) != w_cur) {
+                            w_cur = b0 >> 5;
+                            pg_cur = pg_nxt;
+                            pg_nxt = load_window(w_cur + 1);
+                        }
+                        pg[0] = __shfl_sync(0xffffffffu, pg_cur, (b0 + (lane % bpt)) & 31);
+                        if (lane < nbox && (pg[0] < 0 || pg[0] >= num_pages)) bad = true;
+                    } else {
 #pragma unroll
-                    for (int k = 0; k < 2; ++k) {
-                        const int i = lane + 32 * k;
-                        if (i < nbox) {
-                            const int j = tok0 + i * box_rows;
-                            const int row = (pg[k] << ps_log2) + (j & ps_mask);
-                            tma_load_3d(smem_u32(st + i * box_bytes), &kmap, full, 0, p.g, row,
-                                        policy);
-                            tma_load_3d(smem_u32(st + S::TILE_BYTES + i * box_bytes), &vmap, full,
-                                        0, p.g, row, policy);
+                        for (int k = 0; k < 2; ++k) {
+                            const int i = lane + 32 * k;
+                            if (i < nbox) {
+                                pg[k] = prow[(tok0 + i * box_rows) >> ps_log2];
+                                if (pg[k] < 0 || pg[k] >= num_pages) bad = true;
+                            }
                         }
                     }
+                    bad = __any_sync(0xffffffffu, bad);
+                    const uint32_t bytes = (bad ? 0u : 2u * box_bytes * nbox) + q_bytes;
+                    if (lane == 0) {
+                        flags[s] = bad ? 1 : 0;
+                        mbar_arrive_expect_tx(full, bytes);
+                    }
+                    __syncwarp();
+                    if (!bad) {
+#pragma unroll
+                        for (int k = 0; k < 2; ++k) {
+                            const int i = lane + 32 * k;
+                            if (i < nbox) {
+                                const int j = tok0 + i * box_rows;
+                                const int row = (pg[k] << ps_log2) + (j & ps_mask);
+                                tma_load_3d(smem_u32(st + i * box_bytes), &kmap, full, 0, p.g, row,
+                                            policy);
+                                tma_load_3d(smem_u32(st + S::TILE_BYTES + i * box_bytes), &vmap, full,
+                                            0, p.g, row, policy);
+                            }
+                        }
+                    }
+                } else {
+                    // pages of fewer than 8 tokens: the tile's key rows gathered
+                    // with 16-byte copies (KPI keys per warp instruction), keys
+                    // past the sequence or on a page outside the pool zero-filled;
+                    // each lane's copies arrive on the full barrier as they
+                    // complete, lane 0 adds its own arrival (with q's bytes)
+                    constexpr int CHK = D / 8, KPI = 32 / CHK, NI = T / KPI;
+                    const int b0 = tile * bpt;
+                    if (bpt <= 32 && (b0 >> 5) != w_cur) {
+                        w_cur = b0 >> 5;
+                        pg_cur = pg_nxt;
+                        pg_nxt = load_window(w_cur + 1);
+                    }
+                    int pgs[NI];
+#pragma unroll
+                    for (int m = 0; m < NI; ++m) {
+                        const int key = m * KPI + lane / CHK;
+                        if (bpt <= 32)
+                            pgs[m] = __shfl_sync(0xffffffffu, pg_cur, (b0 + key / box_rows) & 31);
+                        else
+                            pgs[m] = key < ntok ? prow[(tok0 + key) >> ps_log2] : 0;
+                    }
+                    bool bad = false;
+#pragma unroll
+                    for (int m = 0; m < NI; ++m) {
+                        const int key = m * KPI + lane / CHK;
+                        bad |= key < ntok && (pgs[m] < 0 || pgs[m] >= num_pages);
+                    }
+                    bad = __any_sync(0xffffffffu, bad);
+                    if (lane == 0) flags[s] = bad ? 1 : 0;
+#pragma unroll
+                    for (int m = 0; m < NI; ++m) {
+                        const int key = m * KPI + lane / CHK, ch = lane % CHK;
+                        const int j = tok0 + key;
+                        const bool ok_row = key < ntok && pgs[m] >= 0 && pgs[m] < num_pages;
+                        const int64_t row = ok_row ? ((int64_t)pgs[m] << ps_log2) + (j & ps_mask) : 0;
+                        const int64_t off = (row * Hkv + p.g) * D + ch * 8;
+                        const uint32_t dst = smem_u32(st) + (key * D + ch * 8) * 2;
+                        cp_async16(dst, k_cache + off, ok_row ? 16u : 0u);
+                        cp_async16(dst + S::TILE_BYTES, v_cache + off, ok_row ? 16u : 0u);
+                    }
+                    cp_async_arrive_noinc(full);
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_expect_tx(full, q_bytes);
                 }
                 if (first && lane == 0)
                     bulk_load(smem_u32(st + 2 * S::TILE_BYTES),
@@ -788,6 +839,8 @@ static pkv_status launch(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_b
     auto kernel = fz.k_new ? decode_kernel<D, G, true> : decode_kernel<D, G, false>;
     if (pkv_host::launch_dependent(kernel, dim3(grid), dim3(kThreads),
                                    Smem<D, G>::bytes(B), stream, kmap, vmap,
+                                   reinterpret_cast<const __nv_bfloat16 *>(k_cache),
+                                   reinterpret_cast<const __nv_bfloat16 *>(v_cache),
                                    reinterpret_cast<const __nv_bfloat16 *>(q), page_table, pt_stride,
                                    seq_lens, B, Hkv, ps_log2, box_rows, num_pages, scale_log2,
                                    ws_part, ws_prefix, dev_status,
