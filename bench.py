@@ -182,6 +182,15 @@ def to_dev(a, dev):
     return t.to(dev)
 
 
+def prime(stream):
+    """Queue ~0.5 ms of device work ahead of a timed region, so the host has
+    enqueued the first timed launches before the device reaches the start event
+    (with few timed steps, the host's launch latency would otherwise be timed)."""
+    import torch
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(1_000_000)
+
+
 def batch_override(args):
     return {"B": args.batch} if args.batch else {}
 
@@ -224,28 +233,36 @@ def run_gpu(args, rank, world):
             import torch.distributed as dist
             dist.barrier()
 
-    # ---- timed region: K steps, per-step events around the decode call too
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
+    # ---- timed region: K steps back to back (events only around the whole
+    # region, so kv_store and decode keep their programmatic-dependent-launch
+    # overlap)
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
     torch.cuda.synchronize()
     with ClockSampler(dev.index) as clocks:
+        prime(stream)
         with torch.cuda.stream(stream):
             t0.record(stream)
             for i in range(args.steps):
-                pkv.kv_store(k_new, v_new, out_loc, k, v, dev_status=status, stream=stream)
-                ev[i][0].record(stream)
-                pkv.paged_decode_attn(q, k, v, pt, sl, x.scale, workspace=ws, dev_status=status,
-                                      out=out, stream=stream)
-                ev[i][1].record(stream)
+                step()
             t1.record(stream)
         stream.synchronize()
     barrier()
     torch.cuda.synchronize()
     ms = t0.elapsed_time(t1) / args.steps
-    dec_ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
     ms_all = reduce_max(ms, world)
+
+    # ---- the decode call alone (main + merge kernel), back to back: the roofline
+    d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    prime(stream)
+    with torch.cuda.stream(stream):
+        d0.record(stream)
+        for i in range(args.steps):
+            pkv.paged_decode_attn(q, k, v, pt, sl, x.scale, workspace=ws, dev_status=status, out=out,
+                                  stream=stream)
+        d1.record(stream)
+    stream.synchronize()
+    dec_ms = d0.elapsed_time(d1) / args.steps
 
     # ---- end to end through the public API with host buffers
     pin = lambda a: to_dev(a, "cpu").pin_memory()  # noqa: E731
@@ -288,6 +305,7 @@ def run_gpu(args, rank, world):
         stream.synchronize()
         barrier()
         f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        prime(stream)
         f0.record(stream)
         for _ in range(args.steps):
             fused_step()
@@ -298,11 +316,18 @@ def run_gpu(args, rank, world):
 
     # ---- prefill TFLOP/s on the ragged-prefill workload, the long-context decode
     # and the mixed continuous-batching step (rank 0 reports)
-    prefill = long_dec = mixed = None
+    prefill = long_dec = mixed = page_sizes = None
+    legs = set(args.legs.split(",")) if args.legs != "all" else {"prefill", "long_decode", "mixed",
+                                                                   "page_sizes"}
     if rank == 0:
-        prefill = time_prefill(args, dev, stream, bf16_peak, bf16_sus, peak_kind)
-        long_dec = time_long_decode(args, dev, stream, hbm_peak, peak_kind)
-        mixed = time_mixed_step(args, dev, stream)
+        if "prefill" in legs or "page_sizes" in legs:
+            prefill = time_prefill(args, dev, stream, bf16_peak, bf16_sus, peak_kind)
+        if "long_decode" in legs:
+            long_dec = time_long_decode(args, dev, stream, hbm_peak, peak_kind)
+        if "mixed" in legs:
+            mixed = time_mixed_step(args, dev, stream)
+        if "page_sizes" in legs:
+            page_sizes = time_page_sizes(args, dev, stream, prefill, hbm_peak, bf16_peak)
 
     value = world * B_step / (ms_all * 1e-3) / 1e9
     dec_gbs = B_dec / (dec_ms * 1e-3) / 1e9
@@ -354,19 +379,18 @@ def run_gpu(args, rank, world):
         "gpu_launches": 3 * args.steps,
         "clocks": clocks.summary(),
     }
-    if prefill is not None:
-        line["prefill"] = prefill
-        line["long_decode"] = long_dec
-        line["mixed_step"] = mixed
+    for key, val in (("prefill", prefill), ("long_decode", long_dec), ("mixed_step", mixed),
+                     ("page_sizes", page_sizes)):
+        if val is not None:
+            line[key] = val
     return line
 
 
-def time_prefill(args, dev, stream, bf16_peak, bf16_sus, peak_kind):
+def prefill_ms(x, dev, stream, reps, warmup):
+    """Median CUDA-event time of one ragged-prefill call on x, L2 flushed before
+    each repetition."""
     import torch
     import paged_kv_cache_out_gb300 as pkv
-    from synth import make_config
-
-    x = make_config("ragged_prefill", seed=args.seed)
     k, v = to_dev(x.k_cache, dev), to_dev(x.v_cache, dev)
     q, pt, sl, cu = (to_dev(x.q, dev), to_dev(x.page_table, dev), to_dev(x.seq_lens, dev),
                      to_dev(x.cu_seqlens_q, dev))
@@ -376,10 +400,9 @@ def time_prefill(args, dev, stream, bf16_peak, bf16_sus, peak_kind):
     out = torch.empty_like(q)
     pws = pkv.prefill_workspace(dev)
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
-    reps = max(5, args.steps)
     times = []
     with torch.cuda.stream(stream):
-        for i in range(args.warmup + reps):
+        for i in range(warmup + reps):
             flush.zero_()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
@@ -387,10 +410,75 @@ def time_prefill(args, dev, stream, bf16_peak, bf16_sus, peak_kind):
                                    dev_status=status, out=out, stream=stream)
             b.record(stream)
             b.synchronize()
-            if i >= args.warmup:
+            if i >= warmup:
                 times.append(a.elapsed_time(b))
     assert int(status.item()) == 0
-    ms = statistics.median(times)
+    return statistics.median(times)
+
+
+def decode_ms(x, dev, stream, reps, warmup):
+    """Mean CUDA-event time of one decode call on x, calls back to back (the
+    K/V read per call is larger than L2)."""
+    import torch
+    import paged_kv_cache_out_gb300 as pkv
+    k, v = to_dev(x.k_cache, dev), to_dev(x.v_cache, dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    pkv.kv_store(to_dev(x.k_new, dev), to_dev(x.v_new, dev), to_dev(x.out_loc, dev), k, v,
+                 dev_status=status, stream=stream)
+    q, pt, sl = to_dev(x.q, dev), to_dev(x.page_table, dev), to_dev(x.seq_lens, dev)
+    out = torch.empty_like(q)
+    ws = pkv.decode_workspace(x.B, x.Hq, x.Hkv, x.d, dev)
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            pkv.paged_decode_attn(q, k, v, pt, sl, x.scale, workspace=ws, dev_status=status, out=out,
+                                  stream=stream)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        prime(stream)
+        a.record(stream)
+        for _ in range(reps):
+            pkv.paged_decode_attn(q, k, v, pt, sl, x.scale, workspace=ws, dev_status=status, out=out,
+                                  stream=stream)
+        b.record(stream)
+        stream.synchronize()
+    assert int(status.item()) == 0
+    return a.elapsed_time(b) / reps
+
+
+def time_page_sizes(args, dev, stream, prefill16, hbm_peak, bf16_peak):
+    """The engines' two other page layouts: miniVLLM's block_size 256 and
+    mini-sglang's token-granular table (page_size 1), for ragged prefill and the
+    Qwen3 decode layer, next to page_size 16."""
+    import torch
+    from synth import make_config
+    res = {"prefill": {}, "decode": {}}
+    for ps in (256, 1):
+        x = make_config("ragged_prefill", seed=args.seed, page_size=ps)
+        ms = prefill_ms(x, dev, stream, max(5, min(args.steps, 20)), args.warmup)
+        tf = prefill_flops(x) / (ms * 1e-3) / 1e12
+        res["prefill"][f"page_size_{ps}"] = {"tflops": round(tf, 2), "ms": round(ms, 5),
+                                             "frac": round(tf / bf16_peak, 4),
+                                             "vs_page_size_16": round(prefill16["ms"] / ms, 4)}
+        torch.cuda.empty_cache()
+    for ps in (16, 256, 1):
+        x = make_config("qwen3_decode", seed=args.seed, page_size=ps, pt_stride=4096 // ps)
+        ms = decode_ms(x, dev, stream, max(20, min(args.steps, 200)), args.warmup)
+        gbs = decode_bytes(x) / (ms * 1e-3) / 1e9
+        res["decode"][f"page_size_{ps}"] = {"gbs": round(gbs, 2), "ms": round(ms, 5),
+                                            "frac": round(gbs / hbm_peak, 4)}
+        torch.cuda.empty_cache()
+    d16 = res["decode"]["page_size_16"]["ms"]
+    for ps in (256, 1):
+        res["decode"][f"page_size_{ps}"]["vs_page_size_16"] = round(d16 / res["decode"][f"page_size_{ps}"]["ms"], 4)
+    res["workloads"] = ("ragged_prefill and qwen3_decode (seed as the run) laid out with the page size named; "
+                        "vs_page_size_16 = time at page_size 16 / time at this page size")
+    return res
+
+
+def time_prefill(args, dev, stream, bf16_peak, bf16_sus, peak_kind):
+    from synth import make_config
+
+    x = make_config("ragged_prefill", seed=args.seed)
+    ms = prefill_ms(x, dev, stream, max(5, args.steps), args.warmup)
     fl = prefill_flops(x)
     tf = fl / (ms * 1e-3) / 1e12
     return {"workload": "ragged_prefill: 8 requests, n~U[128,2048], prefix 0-50 %, Hq=16, "
@@ -402,33 +490,11 @@ def time_prefill(args, dev, stream, bf16_peak, bf16_sus, peak_kind):
 
 def time_long_decode(args, dev, stream, hbm_peak, peak_kind):
     """Decode call alone on the Llama-3.2-1B-shaped long-context workload."""
-    import torch
-    import paged_kv_cache_out_gb300 as pkv
     from synth import make_config
 
     x = make_config("llama_long_decode", seed=args.seed)
-    k, v = to_dev(x.k_cache, dev), to_dev(x.v_cache, dev)
-    status = torch.zeros(1, dtype=torch.int32, device=dev)
-    pkv.kv_store(to_dev(x.k_new, dev), to_dev(x.v_new, dev), to_dev(x.out_loc, dev), k, v,
-                 dev_status=status, stream=stream)
-    q, pt, sl = to_dev(x.q, dev), to_dev(x.page_table, dev), to_dev(x.seq_lens, dev)
-    out = torch.empty_like(q)
-    ws = pkv.decode_workspace(x.B, x.Hq, x.Hkv, x.d, dev)
-    reps = max(20, min(args.steps, 500))
-    times = []
-    with torch.cuda.stream(stream):
-        for i in range(args.warmup + reps):
-            # back to back: the 0.4 GB of K/V rows read per call is three times L2
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            pkv.paged_decode_attn(q, k, v, pt, sl, x.scale, workspace=ws, dev_status=status,
-                                  out=out, stream=stream)
-            b.record(stream)
-            if i >= args.warmup:
-                times.append((a, b))
-        stream.synchronize()
-    assert int(status.item()) == 0
-    ms = statistics.median(a.elapsed_time(b) for a, b in times)
+    # back to back: the 0.36 GB of K/V rows read per call is three times L2
+    ms = decode_ms(x, dev, stream, max(20, min(args.steps, 500)), args.warmup)
     nb = decode_bytes(x)
     gbs = nb / (ms * 1e-3) / 1e9
     return {"workload": f"llama_long_decode: B={x.B}, Hq={x.Hq}, Hkv={x.Hkv}, d={x.d}, "
@@ -499,6 +565,7 @@ def time_mixed_step(args, dev, stream):
             for _ in range(args.warmup):
                 fn()
             stream.synchronize()
+            prime(stream)
             e0.record(stream)
             for _ in range(reps):
                 fn()
@@ -568,7 +635,26 @@ def oracle_sample(x, target_s: float, threads: int):
         nseq = min(x.B, max(nseq + 1, int(nseq * min(8.0, 1.2 * target_s / max(dt, 1e-3)))))
 
 
-def cpu_baseline(x, target_s=12.0):
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().startswith("Model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith(("model name", "cpu part")):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+def cpu_baseline(x, target_s=10.0):
+    """The oracle on all host cores and on one, each on a sample of about target_s."""
     import oracle
     threads = oracle.max_threads()
     dt, nbytes, nseq = oracle_sample(x, target_s, threads)
@@ -576,10 +662,14 @@ def cpu_baseline(x, target_s=12.0):
     while dt < target_s and nseq == x.B:          # the whole step is quick: repeat it
         more, nb, _ = oracle_sample(x, target_s, threads)
         dt, nbytes, reps = dt + more, nbytes + nb, reps + 1
+    dt1, nbytes1, nseq1 = oracle_sample(x, target_s / 2, 1)
     return {"value": round(nbytes / dt / 1e9, 4), "unit": "GB/s", "cores": threads,
-            "kind": "oracle", "seconds": round(dt, 3),
+            "kind": "oracle", "seconds": round(dt, 3), "cpu_model": cpu_model(),
             "sample": f"kv_store + attention of the first {nseq} of {x.B} sequences, "
-                      f"{reps} time(s) ({nbytes} algorithmic bytes), float64 C, OpenMP over rows"}
+                      f"{reps} time(s) ({nbytes} algorithmic bytes), float64 C, OpenMP over rows",
+            "single_thread": {"value": round(nbytes1 / dt1 / 1e9, 4), "unit": "GB/s",
+                              "seconds": round(dt1, 3),
+                              "sample": f"kv_store + attention of the first {nseq1} of {x.B} sequences"}}
 
 
 def workload_config(args, x):
@@ -644,6 +734,9 @@ def main():
     ap.add_argument("--batch", type=int, default=0,
                     help="number of sequences of the decode workload (default: the workload's own)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--legs", default="all",
+                    help="benchmarks run besides the headline step: all, none, or a comma list of "
+                         "prefill, long_decode, mixed, page_sizes")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

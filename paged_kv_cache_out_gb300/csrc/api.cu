@@ -80,6 +80,22 @@ bool encode_kv_map(CUtensorMap *map, const void *base, int64_t num_slots, int nu
     return r == CUDA_SUCCESS;
 }
 
+bool encode_rows_map(CUtensorMap *map, const void *base, int64_t rows, int head_dim) {
+    auto enc = encoder();
+    // row coordinates of a gather are 32-bit signed
+    if (!enc || rows <= 0 || rows > 0x7fffffffll) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)head_dim, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)head_dim * 2};
+    cuuint32_t box[2] = {(cuuint32_t)head_dim, 1u};
+    cuuint32_t estr[2] = {1u, 1u};
+    const CUtensorMapL2promotion promo = head_dim * 2 >= 256 ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B
+                                                             : CU_TENSOR_MAP_L2_PROMOTION_L2_128B;
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, promo,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 bool encode_q_map(CUtensorMap *map, const void *base, int64_t tokens, int num_q_heads,
                   int head_dim, int box_heads, int box_tokens) {
     auto enc = encoder();

@@ -154,6 +154,20 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
+// Four rows of a 2-D tensor map (rows r0..r3, columns c0 onward, one box
+// width each) into consecutive box-sized pieces of shared memory at dst,
+// completing on an mbarrier; the map's box must be one row high.  Every row
+// coordinate must lie inside the tensor.
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap *map, uint32_t bar, int c0,
+                                            int r0, int r1, int r2, int r3, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes.L2::"
+        "cache_hint [%0], [%1, {%3, %4, %5, %6, %7}], [%2], %8;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3),
+        "l"(policy)
+        : "memory");
+}
+
 // Plain bulk copy global -> shared (16-byte aligned addresses, size a multiple of 16).
 // Prefetch one tile of a tensor map into L2 (no shared memory, no barrier).
 __device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap *map, int c0, int c1, int c2) {
@@ -419,6 +433,11 @@ bool current_device(DeviceInfo *info);
 // swizzle128 selects the 128-byte swizzle (box_inner must then be 64).
 bool encode_kv_map(CUtensorMap *map, const void *base, int64_t num_slots, int num_kv_heads,
                    int head_dim, int box_inner, int box_rows, bool swizzle128);
+
+// Encode a 2-D tensor map over a K or V pool viewed as rows of head_dim bf16
+// (row = slot * num_kv_heads + head), box {head_dim, 1}, no swizzle: the map
+// that tile::gather4 loads take, four arbitrary rows at a time.
+bool encode_rows_map(CUtensorMap *map, const void *base, int64_t rows, int head_dim);
 
 // Encode a 3-D tiled tensor map over q viewed as [tokens, num_q_heads, head_dim]
 // bf16 with box {64, heads, tokens} and the 128-byte swizzle.

@@ -304,11 +304,9 @@ __global__ void __launch_bounds__(kThreads, G <= 4 ? kCtasPerSm : 1)
     grid_dependency_wait();  // the pool rows of this step are written by the kernel before
     allow_dependents();      // the merge kernel may become resident and wait for us
     if (tid == 0) {
-        // full: the producer's arrival with the tx bytes; for pages of fewer
-        // than 8 tokens also one arrival per producer lane when its copies land
-        const uint32_t full_count = box_rows < 8 ? 33u : 1u;
+        // full: the producer's arrival with the tx bytes
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(smem_u32(&bars[s]), full_count);
+            mbar_init(smem_u32(&bars[s]), 1u);
             mbar_init(smem_u32(&bars[STAGES + s]), kConsumerWarps);  // empty: one per consumer warp
         }
         mbar_init(smem_u32(&bars[2 * STAGES]), kConsumerWarps);  // fused stores written
@@ -342,7 +340,8 @@ __global__ void __launch_bounds__(kThreads, G <= 4 ? kCtasPerSm : 1)
         bool ok = true;
         bool stores_seen = false;
         // boxes per tile; up to 32 of them page ids come in warp-wide windows
-        // of 32 boxes, the next window loaded one window ahead
+        // of 32 boxes, the next two windows loaded ahead (with pages of one
+        // token a window lasts one tile)
         const int bpt = T / box_rows;
         while (ok && next_piece(pos, my_end, my_start, prefix, B, Hkv, p)) {
             if (p.t1 <= p.t0) continue;  // lead units only: nothing to load
@@ -353,11 +352,18 @@ __global__ void __launch_bounds__(kThreads, G <= 4 ? kCtasPerSm : 1)
                 return key < L ? prow[key >> ps_log2] : 0;
             };
             int w_cur = (p.t0 * bpt) >> 5;
-            int pg_cur = 0, pg_nxt = 0;
+            int pg_cur = 0, pg_nxt = 0, pg_nxt2 = 0;
             if (bpt <= 32) {
                 pg_cur = load_window(w_cur);
                 pg_nxt = load_window(w_cur + 1);
+                pg_nxt2 = load_window(w_cur + 2);
             }
+            auto advance = [&](int w) {
+                w_cur = w;
+                pg_cur = pg_nxt;
+                pg_nxt = pg_nxt2;
+                pg_nxt2 = load_window(w + 2);
+            };
             for (int tile = p.t0; tile < p.t1; ++tile, ++it) {
                 const int s = it % STAGES;
                 const uint32_t ph = (it / STAGES) & 1;
@@ -389,11 +395,7 @@ __global__ void __launch_bounds__(kThreads, G <= 4 ? kCtasPerSm : 1)
                     bool bad = false;
                     if (bpt <= 32) {
                         const int b0 = tile * bpt;
-                        if ((b0 >> 5) != w_cur) {
-                            w_cur = b0 >> 5;
-                            pg_cur = pg_nxt;
-                            pg_nxt = load_window(w_cur + 1);
-                        }
+                        if ((b0 >> 5) != w_cur) advance(b0 >> 5);
                         pg[0] = __shfl_sync(0xffffffffu, pg_cur, (b0 + (lane % bpt)) & 31);
                         if (lane < nbox && (pg[0] < 0 || pg[0] >= num_pages)) bad = true;
                     } else {
@@ -429,48 +431,42 @@ __global__ void __launch_bounds__(kThreads, G <= 4 ? kCtasPerSm : 1)
                     }
                 } else {
                     // pages of fewer than 8 tokens: the tile's key rows gathered
-                    // with 16-byte copies (KPI keys per warp instruction), keys
-                    // past the sequence or on a page outside the pool zero-filled;
-                    // each lane's copies arrive on the full barrier as they
-                    // complete, lane 0 adds its own arrival (with q's bytes)
-                    constexpr int CHK = D / 8, KPI = 32 / CHK, NI = T / KPI;
+                    // four at a time with TMA (tile::gather4 over the pool viewed
+                    // as rows of one head, row = slot * Hkv + g).  Lane i < NG
+                    // copies K rows 4i..4i+3, lane NG + i the same V rows.  Keys
+                    // past the sequence end take the row of the tile's first key
+                    // (the consumers never use them), so every row read exists.
+                    constexpr int NG = T / 4;  // gathers per tile and tensor
+                    static_assert(2 * NG <= 32, "one gather per lane");
                     const int b0 = tile * bpt;
-                    if (bpt <= 32 && (b0 >> 5) != w_cur) {
-                        w_cur = b0 >> 5;
-                        pg_cur = pg_nxt;
-                        pg_nxt = load_window(w_cur + 1);
-                    }
-                    int pgs[NI];
-#pragma unroll
-                    for (int m = 0; m < NI; ++m) {
-                        const int key = m * KPI + lane / CHK;
-                        if (bpt <= 32)
-                            pgs[m] = __shfl_sync(0xffffffffu, pg_cur, (b0 + key / box_rows) & 31);
-                        else
-                            pgs[m] = key < ntok ? prow[(tok0 + key) >> ps_log2] : 0;
-                    }
+                    if (bpt <= 32 && (b0 >> 5) != w_cur) advance(b0 >> 5);
+                    const int gi = lane % NG;
+                    int rows[4];
                     bool bad = false;
 #pragma unroll
-                    for (int m = 0; m < NI; ++m) {
-                        const int key = m * KPI + lane / CHK;
-                        bad |= key < ntok && (pgs[m] < 0 || pgs[m] >= num_pages);
+                    for (int r = 0; r < 4; ++r) {
+                        const int key = 4 * gi + r;
+                        const int kk = key < ntok ? key : 0;
+                        int pg;
+                        if (bpt <= 32)
+                            pg = __shfl_sync(0xffffffffu, pg_cur, (b0 + kk / box_rows) & 31);
+                        else
+                            pg = prow[(tok0 + kk) >> ps_log2];
+                        if (key < ntok && (pg < 0 || pg >= num_pages)) bad = true;
+                        const int64_t slot = ((int64_t)pg << ps_log2) + ((tok0 + kk) & ps_mask);
+                        rows[r] = static_cast<int>(slot * Hkv + p.g);
                     }
                     bad = __any_sync(0xffffffffu, bad);
-                    if (lane == 0) flags[s] = bad ? 1 : 0;
-#pragma unroll
-                    for (int m = 0; m < NI; ++m) {
-                        const int key = m * KPI + lane / CHK, ch = lane % CHK;
-                        const int j = tok0 + key;
-                        const bool ok_row = key < ntok && pgs[m] >= 0 && pgs[m] < num_pages;
-                        const int64_t row = ok_row ? ((int64_t)pgs[m] << ps_log2) + (j & ps_mask) : 0;
-                        const int64_t off = (row * Hkv + p.g) * D + ch * 8;
-                        const uint32_t dst = smem_u32(st) + (key * D + ch * 8) * 2;
-                        cp_async16(dst, k_cache + off, ok_row ? 16u : 0u);
-                        cp_async16(dst + S::TILE_BYTES, v_cache + off, ok_row ? 16u : 0u);
+                    if (lane == 0) {
+                        flags[s] = bad ? 1 : 0;
+                        mbar_arrive_expect_tx(full, (bad ? 0u : 2u * S::TILE_BYTES) + q_bytes);
                     }
-                    cp_async_arrive_noinc(full);
                     __syncwarp();
-                    if (lane == 0) mbar_arrive_expect_tx(full, q_bytes);
+                    if (!bad && lane < 2 * NG) {
+                        const uint32_t dst = smem_u32(st) + (lane < NG ? 0u : S::TILE_BYTES) + gi * 4 * D * 2;
+                        tma_gather4(dst, lane < NG ? &kmap : &vmap, full, 0, rows[0], rows[1], rows[2],
+                                    rows[3], policy);
+                    }
                 }
                 if (first && lane == 0)
                     bulk_load(smem_u32(st + 2 * S::TILE_BYTES),
@@ -825,9 +821,16 @@ static pkv_status launch(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_b
     const int box_rows = page_size < T ? page_size : T;
     CUtensorMap kmap, vmap;
     const int64_t slots = num_pages * page_size;
-    if (!pkv_host::encode_kv_map(&kmap, k_cache, slots, Hkv, D, D, box_rows, false) ||
-        !pkv_host::encode_kv_map(&vmap, v_cache, slots, Hkv, D, D, box_rows, false))
-        return PKV_EINVAL;
+    if (box_rows >= 8) {  // page boxes
+        if (!pkv_host::encode_kv_map(&kmap, k_cache, slots, Hkv, D, D, box_rows, false) ||
+            !pkv_host::encode_kv_map(&vmap, v_cache, slots, Hkv, D, D, box_rows, false))
+            return PKV_EINVAL;
+    } else {  // rows gathered four at a time
+        if (slots * Hkv > 0x7fffffffll) return PKV_EUNSUPPORTED;
+        if (!pkv_host::encode_rows_map(&kmap, k_cache, slots * Hkv, D) ||
+            !pkv_host::encode_rows_map(&vmap, v_cache, slots * Hkv, D))
+            return PKV_EINVAL;
+    }
     int ps_log2 = 0;
     while ((1 << ps_log2) < page_size) ++ps_log2;
     const int grid = dev.sm_count * ctas;
