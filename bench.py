@@ -502,6 +502,8 @@ def time_long_decode(args, dev, stream, hbm_peak, peak_kind):
             "gbs": round(gbs, 2), "ms": round(ms, 5), "bytes": nb, "peak": hbm_peak,
             "peak_kind": f"{peak_kind} HBM copy GB/s", "frac": round(gbs / hbm_peak, 4),
             "tokens_per_s": round(x.B / (ms * 1e-3), 1),
+            "traffic": profiled_traffic("decode_kernel_llama_long_decode.md",
+                                        source_digest("decode.cu", "common.cuh")),
             "l2": "back-to-back calls; 0.36 GB read per call > 129 MB L2, no flush"}
 
 
