@@ -316,9 +316,9 @@ def run_gpu(args, rank, world):
 
     # ---- prefill TFLOP/s on the ragged-prefill workload, the long-context decode
     # and the mixed continuous-batching step (rank 0 reports)
-    prefill = long_dec = mixed = page_sizes = None
+    prefill = long_dec = mixed = page_sizes = shared_prefix = None
     legs = set(args.legs.split(",")) if args.legs != "all" else {"prefill", "long_decode", "mixed",
-                                                                   "page_sizes"}
+                                                                   "page_sizes", "shared_prefix"}
     if rank == 0:
         if "prefill" in legs or "page_sizes" in legs:
             prefill = time_prefill(args, dev, stream, bf16_peak, bf16_sus, peak_kind)
@@ -328,6 +328,8 @@ def run_gpu(args, rank, world):
             mixed = time_mixed_step(args, dev, stream)
         if "page_sizes" in legs:
             page_sizes = time_page_sizes(args, dev, stream, prefill, hbm_peak, bf16_peak)
+        if "shared_prefix" in legs:
+            shared_prefix = time_shared_prefix(args, dev, stream, bf16_peak)
 
     value = world * B_step / (ms_all * 1e-3) / 1e9
     dec_gbs = B_dec / (dec_ms * 1e-3) / 1e9
@@ -380,15 +382,15 @@ def run_gpu(args, rank, world):
         "clocks": clocks.summary(),
     }
     for key, val in (("prefill", prefill), ("long_decode", long_dec), ("mixed_step", mixed),
-                     ("page_sizes", page_sizes)):
+                     ("page_sizes", page_sizes), ("shared_prefix", shared_prefix)):
         if val is not None:
             line[key] = val
     return line
 
 
-def prefill_ms(x, dev, stream, reps, warmup):
+def prefill_ms(x, dev, stream, reps, warmup, shared=False):
     """Median CUDA-event time of one ragged-prefill call on x, L2 flushed before
-    each repetition."""
+    each repetition (shared: the shared-prefix entry point with x's groups)."""
     import torch
     import paged_kv_cache_out_gb300 as pkv
     k, v = to_dev(x.k_cache, dev), to_dev(x.v_cache, dev)
@@ -398,7 +400,14 @@ def prefill_ms(x, dev, stream, reps, warmup):
     pkv.kv_store(to_dev(x.k_new, dev), to_dev(x.v_new, dev), to_dev(x.out_loc, dev), k, v,
                  dev_status=status, stream=stream)
     out = torch.empty_like(q)
-    pws = pkv.prefill_workspace(dev)
+    if shared:
+        gs = x.meta["prefix_group_start"]
+        gsd, gld = to_dev(gs, dev), to_dev(x.meta["prefix_len"], dev)
+        cu64 = x.cu_seqlens_q.astype("int64")
+        max_group = int(max(cu64[gs[g + 1]] - cu64[gs[g]] for g in range(len(gs) - 1)))
+        pws = pkv.prefill_shared_workspace(x.Tq, x.Hq, x.d, dev)
+    else:
+        pws = pkv.prefill_workspace(dev)
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     times = []
     with torch.cuda.stream(stream):
@@ -406,8 +415,13 @@ def prefill_ms(x, dev, stream, reps, warmup):
             flush.zero_()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
-            pkv.paged_prefill_attn(q, cu, k, v, pt, sl, x.scale, x.max_q_len, workspace=pws,
-                                   dev_status=status, out=out, stream=stream)
+            if shared:
+                pkv.paged_prefill_attn_shared(q, cu, k, v, pt, sl, x.scale, x.max_q_len, gsd, gld,
+                                              max_group, workspace=pws, dev_status=status, out=out,
+                                              stream=stream)
+            else:
+                pkv.paged_prefill_attn(q, cu, k, v, pt, sl, x.scale, x.max_q_len, workspace=pws,
+                                       dev_status=status, out=out, stream=stream)
             b.record(stream)
             b.synchronize()
             if i >= warmup:
@@ -486,6 +500,28 @@ def time_prefill(args, dev, stream, bf16_peak, bf16_sus, peak_kind):
             "tflops": round(tf, 2), "ms": round(ms, 5), "flops": fl,
             "peak": bf16_peak, "peak_kind": f"{peak_kind} bf16 dense burst",
             "frac": round(tf / bf16_peak, 4), "l2": "flushed (512 MB write) before each rep"}
+
+
+def time_shared_prefix(args, dev, stream, bf16_peak):
+    """Many requests after one common cached prefix: the plain prefill (each
+    request reads the shared pages for itself) against the shared-prefix entry
+    point (the group's new tokens packed into dense query tiles that read each
+    shared K/V tile once), same inputs, same useful FLOPs."""
+    from synth import make_config
+
+    x = make_config("shared_prefix_prefill", seed=args.seed)
+    reps = max(5, min(args.steps, 20))
+    ms_plain = prefill_ms(x, dev, stream, reps, args.warmup)
+    ms_shared = prefill_ms(x, dev, stream, reps, args.warmup, shared=True)
+    fl = prefill_flops(x)
+    return {"workload": f"shared_prefix_prefill: {x.B} requests, {int(x.meta['prefix_len'][0])} shared "
+                        f"cached tokens, new tokens U[16,128] ({x.Tq} in all), Hq=16, Hkv=8, d=128, "
+                        f"page_size 16",
+            "ms_plain": round(ms_plain, 5), "ms_shared": round(ms_shared, 5),
+            "speedup": round(ms_plain / ms_shared, 3), "flops": fl,
+            "tflops_shared": round(fl / (ms_shared * 1e-3) / 1e12, 2),
+            "frac_shared": round(fl / (ms_shared * 1e-3) / 1e12 / bf16_peak, 4),
+            "l2": "flushed (512 MB write) before each rep"}
 
 
 def time_long_decode(args, dev, stream, hbm_peak, peak_kind):
@@ -738,7 +774,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--legs", default="all",
                     help="benchmarks run besides the headline step: all, none, or a comma list of "
-                         "prefill, long_decode, mixed, page_sizes")
+                         "prefill, long_decode, mixed, page_sizes, shared_prefix")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -9,6 +9,9 @@
  *                           decode attention (one launch instead of two)
  *   pkv_paged_prefill_attn  ragged causal attention of new tokens over a
  *                           cached prefix plus themselves
+ *   pkv_paged_prefill_attn_shared  the same, for requests that share a cached
+ *                           prefix: each shared key tile is read once for
+ *                           all of a group's new tokens
  *
  * Sources of the operations' meaning:
  *   - mini-sglang "Engine Class": forward_batch takes a batch whose phase is
@@ -84,6 +87,11 @@ typedef enum pkv_status {
 #define PKV_DEV_BAD_WORKSPACE 32  /* prefill: the workspace counters were not zero when the
                                      call started (never cleared, or in use by another call
                                      at the same time); work may have been skipped */
+#define PKV_DEV_BAD_SHARED 64  /* shared-prefix prefill: a prefix group out of range, a
+                                  shared length that is negative, not a whole number of
+                                  pages or longer than a member's cached prefix (that
+                                  request's rows written as NaN), or a member whose
+                                  page-table row does not list the group's shared pages */
 
 /* Human-readable name of a pkv_status value. */
 const char *pkv_status_string(int status);
@@ -239,6 +247,72 @@ pkv_status pkv_paged_prefill_attn(const pkv_bf16 *q, const int32_t *cu_seqlens_q
 
 /* Bytes of device workspace pkv_paged_prefill_attn needs (a small constant). */
 size_t pkv_prefill_workspace_size(void);
+
+/*
+ * paged_prefill_attn_shared: pkv_paged_prefill_attn for a batch in which
+ * groups of requests share their leading cached keys (prefix caching: the
+ * requests' page-table rows list the same physical pages for a common prefix,
+ * which the pool holds once).
+ *
+ * zero-to-sglang "Chapter 1 mini-sglang: What an Inference Engine Looks
+ * Like", the roadmap on prefix caching and RadixAttention: requests that
+ * begin with the same tokens reuse one cached copy of that prefix's KV.
+ * miniVLLM "Engine Architecture", prepare_prefill: block_tables map each
+ * sequence's logical blocks to physical blocks, so several sequences can list
+ * the same blocks.
+ *
+ * The result is that of pkv_paged_prefill_attn on the same arguments (every
+ * new token attends keys 0 .. c_r + i of its own request); only the order of
+ * work differs.  The call runs two passes of the prefill kernel on `stream`:
+ *   1. for each group, the new tokens of all its requests, packed back to
+ *      back, against the group's shared keys (no mask: every new token comes
+ *      after the prefix), so each shared K/V tile is loaded once per 256
+ *      packed query rows rather than once per request; each row's fp32 state
+ *      goes to the workspace;
+ *   2. each request's new tokens against its keys after the shared prefix,
+ *      causally, merged with the row's first-pass state by log-sum-exp.
+ *
+ *   prefix_group_start  [num_prefix_groups + 1] int32, non-decreasing, within
+ *                 [0, batch]: group g is requests prefix_group_start[g] ..
+ *                 prefix_group_start[g+1]-1 (consecutive, so their new tokens
+ *                 are one contiguous range of q); requests in no group attend
+ *                 as in pkv_paged_prefill_attn
+ *   prefix_len    [num_prefix_groups] int32: keys 0 .. prefix_len[g]-1 are
+ *                 shared by the group's requests: a whole number of pages,
+ *                 listed first in each member's page-table row (the first
+ *                 member's row is the one read), and within every member's
+ *                 cached prefix.  0 = nothing shared.
+ *   num_prefix_groups  groups; 0 makes the call pkv_paged_prefill_attn
+ *   max_group_tokens   host upper bound on the new tokens of any one group
+ *                 (sizes the first pass's grid); 0 makes the call
+ *                 pkv_paged_prefill_attn
+ *   workspace     device buffer of at least
+ *                 pkv_prefill_shared_workspace_size(total_q_tokens,
+ *                 num_q_heads, head_dim) bytes, 16-byte aligned; its first
+ *                 pkv_prefill_workspace_size() bytes are the work-queue
+ *                 counters, with the same zero-fill contract as for
+ *                 pkv_paged_prefill_attn; the rest holds the first pass's row
+ *                 states (no initial contents needed)
+ * Other arguments as for pkv_paged_prefill_attn.  Device-detected errors add
+ * PKV_DEV_BAD_SHARED (see above) to those of pkv_paged_prefill_attn.
+ */
+pkv_status pkv_paged_prefill_attn_shared(const pkv_bf16 *q, const int32_t *cu_seqlens_q,
+                                         const pkv_bf16 *k_cache, const pkv_bf16 *v_cache,
+                                         const int32_t *page_table, int64_t page_table_stride,
+                                         const int32_t *seq_lens, int batch,
+                                         int64_t total_q_tokens, int max_q_len,
+                                         int num_q_heads, int num_kv_heads, int head_dim,
+                                         int page_size, int64_t num_pages, float softmax_scale,
+                                         const int32_t *prefix_group_start,
+                                         const int32_t *prefix_len, int num_prefix_groups,
+                                         int max_group_tokens, void *workspace,
+                                         size_t workspace_bytes, int32_t *dev_status,
+                                         pkv_bf16 *out, void *stream);
+
+/* Bytes of device workspace pkv_paged_prefill_attn_shared needs: the work-queue
+ * counters plus (head_dim + 2) fp32 per (new token, query head); 0 for
+ * invalid arguments. */
+size_t pkv_prefill_shared_workspace_size(int64_t total_q_tokens, int num_q_heads, int head_dim);
 
 /*
  * Size of the fixed scratch area that pkv_paged_decode_attn_noalloc uses in

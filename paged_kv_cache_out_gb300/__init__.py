@@ -7,6 +7,7 @@ from .binding import (  # noqa: F401
     DEV_BAD_CUSEQ,
     DEV_BAD_PAGE,
     DEV_BAD_SEQLEN,
+    DEV_BAD_SHARED,
     DEV_BAD_SLOT,
     DEV_BAD_WORKSPACE,
     DEV_TIMEOUT,
@@ -18,5 +19,7 @@ from .binding import (  # noqa: F401
     paged_decode_attn,
     paged_decode_attn_store,
     paged_prefill_attn,
+    paged_prefill_attn_shared,
+    prefill_shared_workspace,
     prefill_workspace,
 )

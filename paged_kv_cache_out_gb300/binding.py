@@ -20,7 +20,7 @@ _lib = None
 
 OK, EINVAL, EUNSUPPORTED, ECUDA = 0, 1, 2, 3
 DEV_BAD_SLOT, DEV_BAD_PAGE, DEV_BAD_SEQLEN, DEV_BAD_CUSEQ, DEV_TIMEOUT = 1, 2, 4, 8, 16
-DEV_BAD_WORKSPACE = 32
+DEV_BAD_WORKSPACE, DEV_BAD_SHARED = 32, 64
 
 _P = ctypes.c_void_p
 _I32, _I64, _F32, _SZ = ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
@@ -37,6 +37,10 @@ SIGNATURES = {
     "pkv_paged_prefill_attn": ([_P, _P, _P, _P, _P, _I64, _P, _I32, _I64, _I32, _I32, _I32,
                                 _I32, _I32, _I64, _F32, _P, _SZ, _P, _P, _P], _I32),
     "pkv_prefill_workspace_size": ([], _SZ),
+    "pkv_paged_prefill_attn_shared": ([_P, _P, _P, _P, _P, _I64, _P, _I32, _I64, _I32, _I32, _I32,
+                                       _I32, _I32, _I64, _F32, _P, _P, _I32, _I32, _P, _SZ, _P, _P,
+                                       _P], _I32),
+    "pkv_prefill_shared_workspace_size": ([_I64, _I32, _I32], _SZ),
     "pkv_paged_decode_attn_noalloc": ([_P, _P, _P, _P, _I64, _P, _I32, _I32, _I32, _I32, _I32,
                                        _I64, _F32, _P, _P, _P], _I32),
 }
@@ -196,4 +200,48 @@ def paged_prefill_attn(q, cu_seqlens_q, k_cache, v_cache, page_table, seq_lens, 
         float(softmax_scale), _ptr(workspace), workspace.numel() * workspace.element_size(),
         _ptr(dev_status), _ptr(out), _stream(stream))
     _check("pkv_paged_prefill_attn", st)
+    return out
+
+
+def prefill_shared_workspace(total_q_tokens, num_q_heads, head_dim, device=None):
+    """A workspace for paged_prefill_attn_shared (its queue counters zeroed)."""
+    n = int(load_library().pkv_prefill_shared_workspace_size(int(total_q_tokens), int(num_q_heads),
+                                                             int(head_dim)))
+    return torch.zeros(max(n, 16), dtype=torch.uint8, device=device or "cuda")
+
+
+def paged_prefill_attn_shared(q, cu_seqlens_q, k_cache, v_cache, page_table, seq_lens,
+                              softmax_scale, max_q_len, prefix_group_start, prefix_len,
+                              max_group_tokens, workspace=None, dev_status=None, out=None,
+                              stream=None):
+    """Ragged causal prefill for requests that share cached prefixes.
+
+    prefix_group_start [n_groups + 1] int32: group g is requests
+    prefix_group_start[g] .. prefix_group_start[g+1]-1; prefix_len [n_groups]
+    int32: the keys they share (whole pages, listed first in every member's
+    page-table row).  max_group_tokens bounds the new tokens of any group.
+    The result equals paged_prefill_attn on the same arguments."""
+    _bf16(q, "q"), _bf16(k_cache, "k_cache"), _bf16(v_cache, "v_cache")
+    _i32(seq_lens, "seq_lens"), _i32(cu_seqlens_q, "cu_seqlens_q")
+    _i32(prefix_group_start, "prefix_group_start"), _i32(prefix_len, "prefix_len")
+    if page_table.dtype != torch.int32 or page_table.dim() != 2 or page_table.stride(1) != 1:
+        raise ValueError("page_table must be a 2-D int32 tensor with unit column stride")
+    Tq, Hq, d = q.shape
+    P, ps, Hkv, d2 = k_cache.shape
+    B = seq_lens.shape[0]
+    n_groups = prefix_len.shape[0]
+    if (d2 != d or v_cache.shape != k_cache.shape or cu_seqlens_q.shape[0] != B + 1
+            or prefix_group_start.shape[0] != n_groups + 1):
+        raise ValueError("shape mismatch")
+    if out is None:
+        out = torch.empty_like(q)
+    if workspace is None:
+        workspace = prefill_shared_workspace(Tq, Hq, d, q.device)
+    st = load_library().pkv_paged_prefill_attn_shared(
+        _ptr(q), _ptr(cu_seqlens_q), _ptr(k_cache), _ptr(v_cache), _ptr(page_table),
+        page_table.stride(0), _ptr(seq_lens), B, Tq, int(max_q_len), Hq, Hkv, d, ps, P,
+        float(softmax_scale), _ptr(prefix_group_start), _ptr(prefix_len), n_groups,
+        int(max_group_tokens), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _ptr(dev_status), _ptr(out), _stream(stream))
+    _check("pkv_paged_prefill_attn_shared", st)
     return out

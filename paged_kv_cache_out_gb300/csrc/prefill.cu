@@ -72,6 +72,15 @@ constexpr int kItemConsumers = 1 + 8 + (kLoaders - 1);  // MMA, softmax and load
 constexpr int kRankGroups = 256;         // up to this many (token block, request) groups
                                          // are ranked by work in the kernel
 constexpr size_t kWorkspaceBytes = 256;  // queue counters (three used, the rest reserved)
+// The shared-prefix form's workspace: the queue counters, then per (token,
+// query head) row its shared-pass running max and sum, then its unnormalised
+// output row (fp32).
+inline size_t ml_bytes(int64_t tokens, int heads) {
+    return ((static_cast<size_t>(tokens) * heads * 2 * 4 + 255) / 256) * 256;
+}
+inline size_t shared_workspace_bytes(int64_t tokens, int heads, int head_dim) {
+    return kWorkspaceBytes + ml_bytes(tokens, heads) + static_cast<size_t>(tokens) * heads * head_dim * 4;
+}
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kNegBig = -1.0e30f;
 constexpr float kRescaleLog2 = 8.0f;  // lazy rescale threshold (factor 256)
@@ -84,9 +93,13 @@ constexpr uint32_t kTmemCols = 512;
 // need more of their registers.  256 x regs_high + 128 x regs_low must not
 // exceed 384 x kRegsLaunch.
 constexpr int kRegsLaunch = 168;
-template <bool SMALL>
+template <bool SMALL, int MODE>
 struct RegSplit {
-    static constexpr int high = SMALL ? 192 : 208, low = SMALL ? 120 : 88;
+    // (measured: 200/104 runs the 128-key pipeline faster than 208/88, whose
+    // loader warps spill; pages of fewer than 8 tokens need still more in the
+    // loaders)
+    static constexpr int high = SMALL ? 176 : 200;
+    static constexpr int low = SMALL ? 152 : 104;
     static_assert(8 * 32 * high + 4 * 32 * low <= kThreads * kRegsLaunch,
                   "register split exceeds the block's registers");
 };
@@ -136,58 +149,130 @@ __device__ __forceinline__ uint32_t swz_offset(int row, int chunk16, int rows) {
     return static_cast<uint32_t>(blk * rows * 128 + row * 128 + ((c ^ (row & 7)) << 4));
 }
 
-// One work item: query tiles A and B of request r, token block mt, KV head g.
+// Passes of the kernel.  kCausal: every request's new tokens against its own
+// keys, causally (the plain prefill).  The two passes of the shared-prefix
+// form split that work for a prefix group (consecutive requests whose first
+// S keys are the same pages):
+//   kShared:  the group's new tokens, packed back to back across its
+//             requests, against the S shared keys; no mask (every new token
+//             comes after the prefix); each row's unnormalised output, running
+//             max and sum go to the workspace;
+//   kPrivate: each request's new tokens against its keys S .. L-1, causally;
+//             the epilogue merges in the row's shared-pass state (log-sum-exp
+//             of the two key ranges) before it normalises and stores.
+enum Mode : int { kCausal = 0, kShared = 1, kPrivate = 2 };
+
+// The prefix groups of a shared-prefix call (null for kCausal).
+struct Groups {
+    const int32_t *start;   // [n + 1]: group g is requests start[g] .. start[g+1]-1
+    const int32_t *len;     // [n]: keys shared by the group's requests
+    int n;
+    int nreq;               // requests in the call
+    float *part_o;          // [Tq * Hq, D] fp32: shared-pass output rows, unnormalised
+    float *part_ml;         // [Tq * Hq, 2] fp32: their running max (log2 domain) and sum
+};
+
+// Group of request r (start[] is non-decreasing; -1 when r is in none).
+__device__ __forceinline__ int group_of(const Groups &gr, int r) {
+    int lo = 0, hi = gr.n;  // find the last g with start[g] <= r
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (gr.start[mid] <= r) lo = mid; else hi = mid;
+    }
+    return (gr.n > 0 && gr.start[lo] <= r && r < gr.start[lo + 1]) ? lo : -1;
+}
+
+// One work item: query tiles A and B of request r (of prefix group r in the
+// shared pass), token block mt, KV head g; key tiles kt0 .. kt0 + n_kt - 1,
+// keys below klo and above a row's limit masked.
 struct Item {
     int r, g, mt;
     int cu0, n, L, c;
     int tbeg[NQ], tend[NQ], nkt[NQ];
-    int n_kt;
+    int n_kt, kt0, klo, pr;  // pr: the request whose page-table row is read
 };
 
-template <int G>
+template <int G, int MODE>
 __device__ __forceinline__ void decode_item(int p, int Hkv, int B, int mtiles, const int *order,
                                             bool ranked, const int32_t *cu_seqlens,
-                                            const int32_t *seq_lens, Item &it) {
+                                            const int32_t *seq_lens, const Groups &gr, Item &it) {
     constexpr int TOK = BM / G;
     const int grank = p / Hkv;
     it.g = p % Hkv;
     const int grp = ranked ? order[grank] : grank;
     it.mt = mtiles - 1 - grp / B;
     it.r = grp % B;
-    it.cu0 = cu_seqlens[it.r];
-    it.n = cu_seqlens[it.r + 1] - it.cu0;
-    it.L = seq_lens[it.r];
-    it.c = it.L - it.n;
+    it.kt0 = 0;
+    it.klo = 0;
+    it.pr = it.r;
+    if constexpr (MODE == kShared) {
+        const int r0 = gr.start[it.r], r1 = gr.start[it.r + 1];
+        it.pr = r0;
+        it.cu0 = cu_seqlens[r0];
+        it.n = cu_seqlens[r1] - it.cu0;
+        it.L = gr.len[it.r];
+        it.c = 0;
+    } else {
+        it.cu0 = cu_seqlens[it.r];
+        it.n = cu_seqlens[it.r + 1] - it.cu0;
+        it.L = seq_lens[it.r];
+        it.c = it.L - it.n;
+        if constexpr (MODE == kPrivate) {
+            const int gi = group_of(gr, it.r);
+            if (gi >= 0) {
+                it.pr = it.r;
+                it.klo = gr.len[gi];
+                it.kt0 = it.klo / BN;
+            }
+        }
+    }
     const int blk_tok0 = it.mt * NQ * TOK;
 #pragma unroll
     for (int qt = 0; qt < NQ; ++qt) {
         it.tbeg[qt] = blk_tok0 + qt * TOK;
         it.tend[qt] = min(it.n, it.tbeg[qt] + TOK);
-        it.nkt[qt] = it.tend[qt] > it.tbeg[qt] ? (it.c + it.tend[qt] + BN - 1) / BN : 0;
+        const int keys = MODE == kShared ? it.L : it.c + it.tend[qt];
+        it.nkt[qt] = it.tend[qt] > it.tbeg[qt] ? (keys + BN - 1) / BN - it.kt0 : 0;
     }
     it.n_kt = it.nkt[0] > it.nkt[1] ? it.nkt[0] : it.nkt[1];
 }
 
-// Work of a (token block, request) group in key tiles: 0 for no tokens, 1 for
-// invalid offsets or lengths (the producer only flags those).
-template <int G>
+// Work of a (token block, request) group in key tiles (a (token block,
+// prefix group) one in the shared pass): 0 for no tokens, 1 for invalid
+// offsets or lengths (the producer only flags those).
+template <int G, int MODE>
 __device__ __forceinline__ int group_weight(int grp, int B, int mtiles, int64_t Tq, int max_q_len,
                                             int64_t cap, const int32_t *cu_seqlens,
-                                            const int32_t *seq_lens) {
+                                            const int32_t *seq_lens, const Groups &gr) {
     constexpr int TOK = BM / G;
     const int mt = mtiles - 1 - grp / B, r = grp % B;
-    const int cu0 = cu_seqlens[r], cu1 = cu_seqlens[r + 1];
-    const int n = cu1 - cu0, L = seq_lens[r];
-    if (cu0 < 0 || n < 0 || cu1 > Tq || (r == 0 && cu0 != 0) || n > max_q_len) return 1;
     const int t0 = mt * NQ * TOK;
-    if (t0 >= n) return 0;
-    if (L - n < 0 || L > cap) return 1;
-    return (L - n + min(n, t0 + NQ * TOK) + BN - 1) / BN;
+    if constexpr (MODE == kShared) {
+        const int r0 = gr.start[r], r1 = gr.start[r + 1], S = gr.len[r];
+        if (r0 < 0 || r1 < r0) return 1;
+        const int n = cu_seqlens[r1] - cu_seqlens[r0];
+        if (t0 >= n || S == 0) return 0;
+        if (S < 0 || S > cap) return 1;
+        return (S + BN - 1) / BN;
+    } else {
+        const int cu0 = cu_seqlens[r], cu1 = cu_seqlens[r + 1];
+        const int n = cu1 - cu0, L = seq_lens[r];
+        if (cu0 < 0 || n < 0 || cu1 > Tq || (r == 0 && cu0 != 0) || n > max_q_len) return 1;
+        if (t0 >= n) return 0;
+        if (L - n < 0 || L > cap) return 1;
+        int kt0 = 0;
+        if constexpr (MODE == kPrivate) {
+            const int gi = group_of(gr, r);
+            if (gi >= 0) kt0 = gr.len[gi] / BN;
+        }
+        const int w = (L - n + min(n, t0 + NQ * TOK) + BN - 1) / BN - kt0;
+        return w > 1 ? w : 1;
+    }
 }
 
 // SMALL: pages of fewer than 8 tokens (gathered key by key); otherwise every
 // page of a tile comes in as TMA boxes.
-template <int D, int G, bool SMALL>
+template <int D, int G, bool SMALL, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                    const __grid_constant__ CUtensorMap vmap, const __nv_bfloat16 *__restrict__ k_cache,
@@ -195,7 +280,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const int32_t *__restrict__ page_table, int64_t pt_stride,
                    const int32_t *__restrict__ seq_lens, int B, int64_t Tq, int max_q_len, int Hkv,
                    int ps_log2, int box_rows, int64_t num_pages, float scale_log2, int mtiles,
-                   unsigned int *sched, int32_t *dev_status, __nv_bfloat16 *__restrict__ out) {
+                   const Groups gr, unsigned int *sched, int32_t *dev_status,
+                   __nv_bfloat16 *__restrict__ out) {
     using Lo = Layout<D>;
     constexpr int TOK = BM / G;  // new tokens per query tile
     const int Hq = Hkv * G;
@@ -272,7 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();  // n_items_s zeroed
     if (ranked) {
         if (tid < n_groups) {
-            const int w = group_weight<G>(tid, B, mtiles, Tq, max_q_len, cap, cu_seqlens, seq_lens);
+            const int w = group_weight<G, MODE>(tid, B, mtiles, Tq, max_q_len, cap, cu_seqlens, seq_lens, gr);
             weight[tid] = w;
             if (w > 0) atomicAdd(const_cast<int *>(n_items_s), 1);
         }
@@ -303,7 +389,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t sV = smem_u32(smem + Lo::OFF_V);
 
     if (warp >= kProducerWarp) {
-    regs_decrease<RegSplit<SMALL>::low>();
+    regs_decrease<RegSplit<SMALL, MODE>::low>();
     if (warp != kMmaWarp) {
         // ================================================================ producer and loaders
         // Warp 8 takes the items and publishes them, and loads the Q tiles;
@@ -367,17 +453,52 @@ __global__ void __launch_bounds__(kThreads, 1)
                     first = false;
                     if (q >= n_items) break;
                     if (lane == 0) *taken_s += 1;
-                    decode_item<G>(q, Hkv, B, mtiles, order, ranked, cu_seqlens, seq_lens, itm);
+                    if constexpr (MODE == kShared) {
+                        const int grp = ranked ? order[q / Hkv] : q / Hkv;
+                        const int gi = grp % B;
+                        const int r0 = gr.start[gi], r1 = gr.start[gi + 1];
+                        if (r0 < 0 || r1 < r0 || r1 > gr.nreq) {
+                            if (lane == 0 && dev_status) atomicOr(dev_status, PKV_DEV_BAD_SHARED);
+                            continue;
+                        }
+                    }
+                    decode_item<G, MODE>(q, Hkv, B, mtiles, order, ranked, cu_seqlens, seq_lens, gr, itm);
                     const int cu1 = itm.cu0 + itm.n;
-                    if (itm.cu0 < 0 || itm.n < 0 || cu1 > Tq || (itm.r == 0 && itm.cu0 != 0) ||
+                    if (itm.cu0 < 0 || itm.n < 0 || cu1 > Tq || (MODE != kShared && itm.r == 0 && itm.cu0 != 0) ||
                         itm.n > max_q_len) {
                         if (lane == 0 && dev_status) atomicOr(dev_status, PKV_DEV_BAD_CUSEQ);
                         continue;
                     }
                     const int blk_tok0 = itm.mt * NQ * TOK;
                     if (blk_tok0 >= itm.n) continue;
-                    if (itm.c < 0 || itm.L > cap) {
-                        if (lane == 0 && dev_status) atomicOr(dev_status, PKV_DEV_BAD_SEQLEN);
+                    if constexpr (MODE == kShared) {
+                        // the shared keys: a whole number of pages, within the table
+                        if (itm.L == 0) continue;
+                        if (itm.L < 0 || itm.L > cap || (itm.L & ((1 << ps_log2) - 1)) != 0) {
+                            if (lane == 0 && dev_status) atomicOr(dev_status, PKV_DEV_BAD_SHARED);
+                            continue;
+                        }
+                    }
+                    // private pass: the shared keys lie inside the request's
+                    // cached prefix, on the same pages as the group's first
+                    // request (checked once per request)
+                    bool bad_share = false;
+                    if constexpr (MODE == kPrivate) {
+                        if (itm.klo < 0 || itm.klo > itm.c || (itm.klo & ((1 << ps_log2) - 1)) != 0) {
+                            bad_share = true;
+                        } else if (itm.klo > 0 && itm.mt == 0 && itm.g == 0) {
+                            const int gi = group_of(gr, itm.r);
+                            const int32_t *row0 = page_table + (int64_t)gr.start[gi] * pt_stride;
+                            const int32_t *rowr = page_table + (int64_t)itm.r * pt_stride;
+                            bool diff = false;
+                            for (int i = lane; i < (itm.klo >> ps_log2); i += 32) diff |= row0[i] != rowr[i];
+                            if (__any_sync(0xffffffffu, diff) && lane == 0 && dev_status)
+                                atomicOr(dev_status, PKV_DEV_BAD_SHARED);
+                        }
+                    }
+                    if (itm.c < 0 || itm.L > cap || bad_share) {
+                        if (lane == 0 && dev_status)
+                            atomicOr(dev_status, bad_share ? PKV_DEV_BAD_SHARED : PKV_DEV_BAD_SEQLEN);
                         const int blk_tok1 = min(itm.n, blk_tok0 + NQ * TOK);
                         for (int idx = lane; idx < (blk_tok1 - blk_tok0) * G * D; idx += 32) {
                             const int t = blk_tok0 + idx / (G * D);
@@ -408,12 +529,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (p < 0) break;
 
-            const int32_t *prow = page_table + (int64_t)itm.r * pt_stride;
-            const int L = itm.L, g = itm.g;
+            const int32_t *prow = page_table + (int64_t)(MODE == kShared ? itm.pr : itm.r) * pt_stride;
+            const int L = itm.L, g = itm.g, kt0 = MODE == kPrivate ? itm.kt0 : 0;
+            // j below counts the item's key tiles; its keys start at (kt0 + j) BN
             auto load_ids = [&](int j, int *dstp) {
 #pragma unroll
                 for (int r = 0; r < 4; ++r) {
-                    const int kk = j * BN + r * 32 + lane;
+                    const int kk = (kt0 + j) * BN + r * 32 + lane;
                     dstp[r] = kk < L ? prow[kk >> ps_log2] : 0;
                 }
             };
@@ -422,12 +544,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int key = (32 * w + lane) * box_rows;
                 return (!SMALL && key < L) ? prow[key >> ps_log2] : 0;
             };
-            int w_cur = 0;
-            int pg_cur = load_window(0), pg_nxt = load_window(1);
+            int w_cur = (kt0 * bpt) >> 5;
+            int pg_cur = load_window(w_cur), pg_nxt = load_window(w_cur + 1);
             // page id of page box pb of tile j (lanes past the tile's boxes get
             // a neighbour's id, unused)
             auto page_of = [&](int j, int pb) -> int {
-                const int b0 = j * bpt;
+                const int b0 = (kt0 + j) * bpt;
                 if ((b0 >> 5) != w_cur) {
                     w_cur = b0 >> 5;
                     pg_cur = pg_nxt;
@@ -444,7 +566,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t full = BAR(kv ? B_VFULL(s) : B_KFULL(s));
                 const uint32_t empty = BAR(kv ? B_VEMPTY(s) : B_KEMPTY(s));
                 const uint32_t dst = (kv ? sV : sK) + s * Lo::KV_BYTES;
-                const int key0 = j * BN;
+                const int key0 = (kt0 + j) * BN;
                 const int nkeys = min(BN, L - key0);  // keys of this tile that exist in pages
                 if (t >= static_cast<uint32_t>(ns) && !mbar_wait_warp(empty, ph ^ 1, abort_flag, dev_status))
                     return false;
@@ -545,10 +667,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                             tma_prefetch_3d(&qmap, blk * 64, g * G, itm.cu0 + itm.tbeg[qt]);
                 }
                 if (!SMALL) {
-                    const int nbox0 = (min(BN, L) + box_rows - 1) / box_rows;
+                    const int nbox0 = (min(BN, L - kt0 * BN) + box_rows - 1) / box_rows;
                     const int pg0 = page_of(0, lane);
                     if (lane < nbox0 && pg0 >= 0 && pg0 < num_pages) {
-                        const int row = (pg0 << ps_log2) + ((lane * box_rows) & ps_mask);
+                        const int row = (pg0 << ps_log2) + ((kt0 * BN + lane * box_rows) & ps_mask);
 #pragma unroll
                         for (int blk = 0; blk < NBLK; ++blk) {
                             tma_prefetch_3d(&kmap, blk * 64, g, row);
@@ -637,11 +759,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ok = false;
                     break;
                 }
-                if (j == n_kt - 1 && (j + 1) * BN > L) {
+                const int kt0 = MODE == kPrivate ? itm.kt0 : 0;
+                if (j == n_kt - 1 && (kt0 + j + 1) * BN > L) {
                     // keys past the sequence end hold stale pool data (maybe NaN):
                     // zero those V rows so that P = 0 there contributes exactly 0
                     const uint32_t vb = sV + s * Lo::KV_BYTES;
-                    const int first_dead = L - j * BN;
+                    const int first_dead = L - (kt0 + j) * BN;
                     for (int idx = lane; idx < (BN - first_dead) * (D / 8); idx += 32) {
                         const int key = first_dead + idx / (D / 8), ch = idx % (D / 8);
                         *reinterpret_cast<uint4 *>(smem + (vb - smem_u32(smem)) +
@@ -708,7 +831,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     } else {
         // ================================================================ softmax
-        regs_increase<RegSplit<SMALL>::high>();
+        regs_increase<RegSplit<SMALL, MODE>::high>();
         const int qt = warp >> 2;                  // query tile of this warpgroup
         const int row = tid & 127;                 // TMEM lane == tile row
         const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
@@ -724,9 +847,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int tok = (qt ? itm.tbeg[1] : itm.tbeg[0]) + row / G;
             const bool row_valid = tok < (qt ? itm.tend[1] : itm.tend[0]);
             const bool warp_live = __any_sync(0xffffffffu, row_valid);
-            const int lim = itm.c + tok;  // last key this row may see
+            // last key this row may see: its own position, or in the shared
+            // pass the last shared key
+            const int lim = MODE == kShared ? itm.L - 1 : itm.c + tok;
             const int my_kt = (qt ? itm.nkt[1] : itm.nkt[0]);
             float m_ref = kNegBig, l_sum = 0.f;
+            if constexpr (MODE == kPrivate) {
+                // the row's shared-pass state, read by the epilogue: into L2 now
+                if (itm.klo > 0 && row_valid) {
+                    const int64_t hrow = (int64_t)(itm.cu0 + tok) * Hq + (int64_t)itm.g * G + row % G;
+                    const char *po = reinterpret_cast<const char *>(gr.part_o + hrow * D);
+#pragma unroll
+                    for (int b = 0; b < D * 4 / 128; ++b) prefetch_l2(po + 128 * b);
+                    prefetch_l2(gr.part_ml + 2 * hrow);
+                }
+            }
             // tcgen05.ld/st are warp-collective: every wait outcome is warp-uniform
             for (int j = 0; j < my_kt; ++j) {
                 // S(j) complete implies PV(j-1) complete: O is stable and P free
@@ -746,12 +881,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // used (their output is not stored, and each row of P only
                     // feeds the same row of O), so a warp holding such rows does
                     // not pay for masking on every tile.
-                    const int key0 = j * BN;
+                    const int key0 = ((MODE == kPrivate ? itm.kt0 : 0) + j) * BN;
                     const int nvalid = row_valid ? lim - key0 + 1 : BN;  // keys kept in this row
-                    if (__any_sync(0xffffffffu, nvalid < BN)) {
+                    // private pass: the shared keys below klo are the shared pass's
+                    const int nlow = MODE == kPrivate ? itm.klo - key0 : 0;  // keys dropped below
+                    if (__any_sync(0xffffffffu, nvalid < BN || nlow > 0)) {
 #pragma unroll
                         for (int i = 0; i < BN; ++i)
-                            if (i >= nvalid) sv[i] = __float_as_uint(-INFINITY);
+                            if (i >= nvalid || i < nlow) sv[i] = __float_as_uint(-INFINITY);
                     }
                     // the row max, then p = 2^(s*scale*log2e - m_ref) on the SFU, packed
                     // to bf16 pairs and written 32 keys at a time into tensor memory
@@ -816,27 +953,80 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ++od;
                 if (!ok) break;
                 tc_fence_after();
-                // the output row out of tensor memory 32 columns at a time,
-                // normalised, packed to bf16 and stored by its own thread in
-                // 32-byte pieces (whole sectors)
                 const bool poison = (bad_flag[slot] != 0) || (*abort_flag != 0);
-                const float inv = row_valid ? 1.f / l_sum : 0.f;
-                const int64_t out_row = ((int64_t)(itm.cu0 + tok) * Hq + (int64_t)itm.g * G + row % G) * D;
-                if (warp_live) {
+                const int64_t hrow = (int64_t)(itm.cu0 + tok) * Hq + (int64_t)itm.g * G + row % G;
+                if constexpr (MODE == kShared) {
+                    // the row's state goes to the workspace for the private pass:
+                    // the output row unnormalised, the running max and sum (a
+                    // poisoned row's sum is NaN, which carries into its output)
+                    if (warp_live) {
 #pragma unroll
-                    for (int cc = 0; cc < D / 32; ++cc) {
-                        uint32_t ov[32];
-                        tmem_ld_32cols(tm_o(qt) + lane_off + cc * 32, ov);
-                        tmem_wait_ld();
-                        uint32_t pk[16];
+                        for (int cc = 0; cc < D / 32; ++cc) {
+                            uint32_t ov[32];
+                            tmem_ld_32cols(tm_o(qt) + lane_off + cc * 32, ov);
+                            tmem_wait_ld();
+                            if (row_valid) {
+                                float4 *dst = reinterpret_cast<float4 *>(gr.part_o + hrow * D + cc * 32);
 #pragma unroll
-                        for (int e = 0; e < 32; e += 2)
-                            pk[e / 2] = poison ? 0x7fc07fc0u  // two bf16 NaNs
-                                               : pack_bf16x2(__uint_as_float(ov[e]) * inv,
-                                                             __uint_as_float(ov[e + 1]) * inv);
-                        if (row_valid) {
-                            st_global_32B(out + out_row + cc * 32, pk);
-                            st_global_32B(out + out_row + cc * 32 + 16, pk + 8);
+                                for (int e = 0; e < 8; ++e)
+                                    dst[e] = make_float4(__uint_as_float(ov[4 * e]), __uint_as_float(ov[4 * e + 1]),
+                                                         __uint_as_float(ov[4 * e + 2]),
+                                                         __uint_as_float(ov[4 * e + 3]));
+                            }
+                        }
+                    }
+                    if (row_valid) {
+                        gr.part_ml[2 * hrow] = m_ref;
+                        gr.part_ml[2 * hrow + 1] = poison ? __int_as_float(0x7fc00000) : l_sum;
+                    }
+                } else {
+                    // the output row out of tensor memory 32 columns at a time,
+                    // normalised, packed to bf16 and stored by its own thread in
+                    // 32-byte pieces (whole sectors).  In the private pass the
+                    // shared pass's state of the row is folded in first: both
+                    // are relative to their own running max (log2 domain), so
+                    // each is weighted by 2^(its max - the larger max).
+                    float w_own = 1.f, w_sh = 0.f, denom = l_sum;
+                    const float4 *osh = nullptr;
+                    if (MODE == kPrivate && itm.klo > 0 && row_valid) {
+                        const float m1 = __ldg(gr.part_ml + 2 * hrow), l1 = __ldg(gr.part_ml + 2 * hrow + 1);
+                        const float mx = fmaxf(m1, m_ref);
+                        w_sh = ex2(m1 - mx);
+                        w_own = ex2(m_ref - mx);
+                        denom = l1 * w_sh + l_sum * w_own;
+                        osh = reinterpret_cast<const float4 *>(gr.part_o + hrow * D);
+                    }
+                    const float inv = row_valid ? 1.f / denom : 0.f;
+                    const float c_own = w_own * inv, c_sh = w_sh * inv;
+                    const int64_t out_row = hrow * D;
+                    if (warp_live) {
+#pragma unroll
+                        for (int cc = 0; cc < D / 32; ++cc) {
+                            uint32_t ov[32];
+                            tmem_ld_32cols(tm_o(qt) + lane_off + cc * 32, ov);
+                            tmem_wait_ld();
+                            float o[32];
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) o[e] = __uint_as_float(ov[e]) * c_own;
+                            if (osh) {
+#pragma unroll
+                                for (int e = 0; e < 8; ++e) {
+                                    const float4 v = __ldg(osh + cc * 8 + e);
+                                    o[4 * e] += v.x * c_sh;
+                                    o[4 * e + 1] += v.y * c_sh;
+                                    o[4 * e + 2] += v.z * c_sh;
+                                    o[4 * e + 3] += v.w * c_sh;
+                                }
+                            }
+                            uint32_t pk[16];
+#pragma unroll
+                            for (int e = 0; e < 32; e += 2)
+                                pk[e / 2] = poison ? 0x7fc07fc0u  // two bf16 NaNs
+                                                   : pack_bf16x2(o[e], o[e + 1]);
+                            if (row_valid) {
+                                st_global_32B(out + out_row + cc * 32, pk);
+                                st_global_32B(out + out_row + cc * 32 + 16, pk + 8);
+                            }
                         }
                     }
                 }
@@ -880,16 +1070,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int D, int G>
+template <int D, int G, int MODE>
 static bool prepare(const pkv_host::DeviceInfo &dev) {
     static std::mutex mu;
     static bool ready[64] = {};
     std::lock_guard<std::mutex> lk(mu);
     if (!ready[dev.device]) {
         if (Layout<D>::bytes() > static_cast<size_t>(dev.max_smem_optin)) return false;
-        if (cudaFuncSetAttribute(prefill_kernel<D, G, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(prefill_kernel<D, G, false, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(Layout<D>::bytes())) != cudaSuccess ||
-            cudaFuncSetAttribute(prefill_kernel<D, G, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            cudaFuncSetAttribute(prefill_kernel<D, G, true, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(Layout<D>::bytes())) != cudaSuccess)
             return false;
         ready[dev.device] = true;
@@ -897,15 +1087,17 @@ static bool prepare(const pkv_host::DeviceInfo &dev) {
     return true;
 }
 
-template <int D, int G>
+// One pass over B work units (requests, or prefix groups in the shared pass)
+// whose new tokens number at most max_q_len each.
+template <int D, int G, int MODE>
 static pkv_status launch(const pkv_bf16 *q, const int32_t *cu, const pkv_bf16 *k_cache,
                          const pkv_bf16 *v_cache, const int32_t *page_table, int64_t pt_stride,
                          const int32_t *seq_lens, int B, int64_t Tq, int max_q_len, int Hkv,
-                         int page_size, int64_t num_pages, float scale, unsigned int *sched,
-                         int32_t *dev_status, pkv_bf16 *out, cudaStream_t stream) {
+                         int page_size, int64_t num_pages, float scale, const Groups &gr,
+                         unsigned int *sched, int32_t *dev_status, pkv_bf16 *out, cudaStream_t stream) {
     pkv_host::DeviceInfo dev;
     if (!pkv_host::current_device(&dev)) return PKV_ECUDA;
-    if (!prepare<D, G>(dev)) return PKV_ECUDA;
+    if (!prepare<D, G, MODE>(dev)) return PKV_ECUDA;
     constexpr int TOK = BM / G;
     const int Hq = Hkv * G;
     const int box_rows = page_size < BN ? page_size : BN;
@@ -917,7 +1109,7 @@ static pkv_status launch(const pkv_bf16 *q, const int32_t *cu, const pkv_bf16 *k
             !pkv_host::encode_kv_map(&vmap, v_cache, slots, Hkv, D, 64, box_rows, true))
             return PKV_EINVAL;
     } else {
-        kmap = qmap;  // unused: small pages are gathered by the producer's lanes
+        kmap = qmap;  // unused: small pages are gathered by the loaders' lanes
         vmap = qmap;
     }
     int ps_log2 = 0;
@@ -928,32 +1120,28 @@ static pkv_status launch(const pkv_bf16 *q, const int32_t *cu, const pkv_bf16 *k
     if (items > 0x7fffffffll) return PKV_EUNSUPPORTED;
     // persistent: one block per SM (fewer when there are fewer items)
     const int grid = items < dev.sm_count ? static_cast<int>(items) : dev.sm_count;
-    auto kernel = box_rows >= 8 ? prefill_kernel<D, G, false> : prefill_kernel<D, G, true>;
+    auto kernel = box_rows >= 8 ? prefill_kernel<D, G, false, MODE> : prefill_kernel<D, G, true, MODE>;
     kernel<<<static_cast<unsigned>(grid), kThreads, Layout<D>::bytes(), stream>>>(
         qmap, kmap, vmap, reinterpret_cast<const __nv_bfloat16 *>(k_cache),
         reinterpret_cast<const __nv_bfloat16 *>(v_cache), cu, page_table, pt_stride, seq_lens, B, Tq,
-        max_q_len, Hkv, ps_log2, box_rows, num_pages, scale * kLog2e, mtiles, sched, dev_status,
+        max_q_len, Hkv, ps_log2, box_rows, num_pages, scale * kLog2e, mtiles, gr, sched, dev_status,
         reinterpret_cast<__nv_bfloat16 *>(out));
     return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ECUDA;
 }
 
-}  // namespace prefill
-}  // namespace pkv
-
-extern "C" size_t pkv_prefill_workspace_size(void) { return pkv::prefill::kWorkspaceBytes; }
-
-extern "C" pkv_status pkv_paged_prefill_attn(const pkv_bf16 *q, const int32_t *cu_seqlens_q,
-                                             const pkv_bf16 *k_cache, const pkv_bf16 *v_cache,
-                                             const int32_t *page_table, int64_t page_table_stride,
-                                             const int32_t *seq_lens, int batch,
-                                             int64_t total_q_tokens, int max_q_len,
-                                             int num_q_heads, int num_kv_heads, int head_dim,
-                                             int page_size, int64_t num_pages, float softmax_scale,
-                                             void *workspace, size_t workspace_bytes,
-                                             int32_t *dev_status, pkv_bf16 *out, void *stream) {
-    using namespace pkv::prefill;
+// Both entry points: argument checks, then the plain causal pass (no groups)
+// or the shared pass followed by the private pass.
+static pkv_status prefill_entry(const pkv_bf16 *q, const int32_t *cu_seqlens_q, const pkv_bf16 *k_cache,
+                                const pkv_bf16 *v_cache, const int32_t *page_table,
+                                int64_t page_table_stride, const int32_t *seq_lens, int batch,
+                                int64_t total_q_tokens, int max_q_len, int num_q_heads, int num_kv_heads,
+                                int head_dim, int page_size, int64_t num_pages, float softmax_scale,
+                                const int32_t *group_start, const int32_t *group_len, int num_groups,
+                                int max_group_tokens, void *workspace, size_t workspace_bytes,
+                                int32_t *dev_status, pkv_bf16 *out, void *stream) {
     if (batch < 0 || total_q_tokens < 0 || max_q_len < 0 || num_q_heads <= 0 || num_kv_heads <= 0 ||
-        num_pages <= 0 || page_table_stride < 0 || page_size <= 0)
+        num_pages <= 0 || page_table_stride < 0 || page_size <= 0 || num_groups < 0 ||
+        max_group_tokens < 0)
         return PKV_EINVAL;
     if (num_q_heads % num_kv_heads != 0) return PKV_EINVAL;
     if (!(softmax_scale == softmax_scale)) return PKV_EINVAL;
@@ -961,6 +1149,8 @@ extern "C" pkv_status pkv_paged_prefill_attn(const pkv_bf16 *q, const int32_t *c
     if (!q || !cu_seqlens_q || !k_cache || !v_cache || !page_table || !seq_lens || !out ||
         !workspace)
         return PKV_EINVAL;
+    const bool shared = num_groups > 0 && max_group_tokens > 0;
+    if (shared && (!group_start || !group_len)) return PKV_EINVAL;
     const int G = num_q_heads / num_kv_heads;
     if (head_dim != 64 && head_dim != 128) return PKV_EUNSUPPORTED;
     if (G != 1 && G != 2 && G != 4 && G != 8) return PKV_EUNSUPPORTED;
@@ -968,16 +1158,38 @@ extern "C" pkv_status pkv_paged_prefill_attn(const pkv_bf16 *q, const int32_t *c
     if (!pkv_host::aligned16(q) || !pkv_host::aligned16(k_cache) || !pkv_host::aligned16(v_cache) ||
         !pkv_host::aligned16(out) || !pkv_host::aligned16(workspace))
         return PKV_EINVAL;
-    if (workspace_bytes < kWorkspaceBytes) return PKV_EINVAL;
+    const size_t need = shared ? shared_workspace_bytes(total_q_tokens, num_q_heads, head_dim)
+                               : kWorkspaceBytes;
+    if (workspace_bytes < need) return PKV_EINVAL;
     if (num_pages * page_size > 0x7fffffffll || total_q_tokens > 0x7fffffffll)
         return PKV_EUNSUPPORTED;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-#define PKV_PREFILL_CASE(DD, GG)                                                                   \
-    if (head_dim == DD && G == GG)                                                                 \
-        return launch<DD, GG>(q, cu_seqlens_q, k_cache, v_cache, page_table, page_table_stride,    \
-                              seq_lens, batch, total_q_tokens, max_q_len, num_kv_heads, page_size, \
-                              num_pages, softmax_scale, static_cast<unsigned int *>(workspace), \
-                              dev_status, out, st);
+    unsigned int *sched = static_cast<unsigned int *>(workspace);
+    Groups gr{group_start, group_len, shared ? num_groups : 0, batch, nullptr, nullptr};
+    if (shared) {
+        uint8_t *w = static_cast<uint8_t *>(workspace);
+        const size_t ml = ml_bytes(total_q_tokens, num_q_heads);
+        gr.part_ml = reinterpret_cast<float *>(w + kWorkspaceBytes);
+        gr.part_o = reinterpret_cast<float *>(w + kWorkspaceBytes + ml);
+    }
+#define PKV_PREFILL_CASE(DD, GG)                                                                      \
+    if (head_dim == DD && G == GG) {                                                                  \
+        if (!shared)                                                                                  \
+            return launch<DD, GG, kCausal>(q, cu_seqlens_q, k_cache, v_cache, page_table,              \
+                                           page_table_stride, seq_lens, batch, total_q_tokens,         \
+                                           max_q_len, num_kv_heads, page_size, num_pages,              \
+                                           softmax_scale, gr, sched, dev_status, out, st);            \
+        pkv_status r1 = launch<DD, GG, kShared>(q, cu_seqlens_q, k_cache, v_cache, page_table,        \
+                                                page_table_stride, seq_lens, num_groups,              \
+                                                total_q_tokens, max_group_tokens, num_kv_heads,       \
+                                                page_size, num_pages, softmax_scale, gr, sched,       \
+                                                dev_status, out, st);                                 \
+        if (r1 != PKV_OK) return r1;                                                                  \
+        return launch<DD, GG, kPrivate>(q, cu_seqlens_q, k_cache, v_cache, page_table,                 \
+                                        page_table_stride, seq_lens, batch, total_q_tokens,            \
+                                        max_q_len, num_kv_heads, page_size, num_pages, softmax_scale,  \
+                                        gr, sched, dev_status, out, st);                              \
+    }
     PKV_PREFILL_CASE(128, 1)
     PKV_PREFILL_CASE(128, 2)
     PKV_PREFILL_CASE(128, 4)
@@ -988,4 +1200,45 @@ extern "C" pkv_status pkv_paged_prefill_attn(const pkv_bf16 *q, const int32_t *c
     PKV_PREFILL_CASE(64, 8)
 #undef PKV_PREFILL_CASE
     return PKV_EUNSUPPORTED;
+}
+
+}  // namespace prefill
+}  // namespace pkv
+
+extern "C" size_t pkv_prefill_workspace_size(void) { return pkv::prefill::kWorkspaceBytes; }
+
+extern "C" size_t pkv_prefill_shared_workspace_size(int64_t total_q_tokens, int num_q_heads, int head_dim) {
+    if (total_q_tokens < 0 || num_q_heads <= 0 || head_dim <= 0) return 0;
+    return pkv::prefill::shared_workspace_bytes(total_q_tokens, num_q_heads, head_dim);
+}
+
+extern "C" pkv_status pkv_paged_prefill_attn(const pkv_bf16 *q, const int32_t *cu_seqlens_q,
+                                             const pkv_bf16 *k_cache, const pkv_bf16 *v_cache,
+                                             const int32_t *page_table, int64_t page_table_stride,
+                                             const int32_t *seq_lens, int batch,
+                                             int64_t total_q_tokens, int max_q_len,
+                                             int num_q_heads, int num_kv_heads, int head_dim,
+                                             int page_size, int64_t num_pages, float softmax_scale,
+                                             void *workspace, size_t workspace_bytes,
+                                             int32_t *dev_status, pkv_bf16 *out, void *stream) {
+    return pkv::prefill::prefill_entry(q, cu_seqlens_q, k_cache, v_cache, page_table, page_table_stride,
+                                       seq_lens, batch, total_q_tokens, max_q_len, num_q_heads,
+                                       num_kv_heads, head_dim, page_size, num_pages, softmax_scale,
+                                       nullptr, nullptr, 0, 0, workspace, workspace_bytes, dev_status,
+                                       out, stream);
+}
+
+extern "C" pkv_status pkv_paged_prefill_attn_shared(
+    const pkv_bf16 *q, const int32_t *cu_seqlens_q, const pkv_bf16 *k_cache, const pkv_bf16 *v_cache,
+    const int32_t *page_table, int64_t page_table_stride, const int32_t *seq_lens, int batch,
+    int64_t total_q_tokens, int max_q_len, int num_q_heads, int num_kv_heads, int head_dim,
+    int page_size, int64_t num_pages, float softmax_scale, const int32_t *prefix_group_start,
+    const int32_t *prefix_len, int num_prefix_groups, int max_group_tokens, void *workspace,
+    size_t workspace_bytes, int32_t *dev_status, pkv_bf16 *out, void *stream) {
+    return pkv::prefill::prefill_entry(q, cu_seqlens_q, k_cache, v_cache, page_table, page_table_stride,
+                                       seq_lens, batch, total_q_tokens, max_q_len, num_q_heads,
+                                       num_kv_heads, head_dim, page_size, num_pages, softmax_scale,
+                                       prefix_group_start, prefix_len, num_prefix_groups,
+                                       max_group_tokens, workspace, workspace_bytes, dev_status, out,
+                                       stream);
 }

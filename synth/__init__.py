@@ -7,6 +7,7 @@ path can consume the same inputs without sharing any computation.
 """
 from .workloads import (  # noqa: F401
     CONFIGS,
+    share_prefix,
     PagedInputs,
     bf16_bits_to_f32,
     f32_to_bf16_bits,

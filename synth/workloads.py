@@ -295,12 +295,61 @@ def _mixed_step(seed, n_chunks=4, chunk_tokens=1024, n_decode=256, **kw):
     return x
 
 
+def share_prefix(x: PagedInputs, groups) -> PagedInputs:
+    """Make groups of consecutive requests share their leading cached pages.
+
+    ``groups`` lists ``(first, end, shared_tokens)``: requests first..end-1
+    take the first ``shared_tokens // page_size`` page ids of request
+    ``first``'s row, the way a prefix cache lets several requests point at
+    one cached copy of a common prefix (zero-to-sglang chapter 1, roadmap on
+    prefix caching; miniVLLM prepare_prefill, block_tables shared across
+    sequences).  ``shared_tokens`` must be a whole number of pages within
+    every member's cached prefix, so the new tokens' slots are untouched.
+    The pages the members held before stay in the pool, unreferenced.  The
+    groups are recorded in ``x.meta`` as ``prefix_group_start`` ([n + 1]) and
+    ``prefix_len`` ([n]) int32 arrays.
+    """
+    ps = x.page_size
+    pt = x.page_table.copy()
+    starts, lens = [], []
+    for first, end, shared in groups:
+        assert shared % ps == 0 and first < end
+        assert (x.prefix_lens[first:end] >= shared).all()
+        pt[first + 1:end, :shared // ps] = pt[first, :shared // ps]
+        if starts and starts[-1] != first:
+            raise ValueError("groups must be consecutive and in request order")
+        if not starts:
+            starts.append(first)
+        starts.append(end)
+        lens.append(shared)
+    x.page_table = pt
+    x.meta["prefix_group_start"] = np.asarray(starts, dtype=np.int32)
+    x.meta["prefix_len"] = np.asarray(lens, dtype=np.int32)
+    return x
+
+
+def _shared_prefix_prefill(seed, B=128, prefix=2048, n_lo=16, n_hi=128, **kw):
+    """Many requests after one common cached prefix (a shared system prompt):
+    ``prefix`` cached tokens on the same pages for all B requests, then each
+    request's own new tokens, uniform in n_lo..n_hi."""
+    rng = np.random.default_rng(seed)
+    n = rng.integers(n_lo, n_hi + 1, size=B)
+    args = dict(Hq=16, Hkv=8, d=128, page_size=16, new_lens=n,
+                prefix_lens=np.full(B, prefix, np.int64), pool_factor=1.1)
+    args.update(kw)
+    x = make_inputs(seed=seed, rng=rng, **args)
+    x = share_prefix(x, [(0, B, prefix)])
+    x.meta.update(name="shared_prefix_prefill", phase="prefill")
+    return x
+
+
 CONFIGS = {
     "tiny_decode": _tiny_decode,
     "qwen3_decode": _qwen3_decode,
     "llama_long_decode": _llama_long_decode,
     "ragged_prefill": _ragged_prefill,
     "mixed_step": _mixed_step,
+    "shared_prefix_prefill": _shared_prefix_prefill,
 }
 
 

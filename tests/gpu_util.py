@@ -53,6 +53,18 @@ class Run:
                                       self.seq_lens, self.x.scale, self.x.max_q_len,
                                       dev_status=self.status, **kw)
 
+    def prefill_shared(self, group_start=None, prefix_len=None, **kw):
+        """The shared-prefix prefill with the groups recorded in x.meta (or given)."""
+        gs = np.asarray(self.x.meta["prefix_group_start"] if group_start is None else group_start,
+                        np.int32)
+        gl = np.asarray(self.x.meta["prefix_len"] if prefix_len is None else prefix_len, np.int32)
+        cu = self.x.cu_seqlens_q.astype(np.int64)
+        max_group = max([int(cu[gs[g + 1]] - cu[gs[g]]) for g in range(len(gl))] + [0])
+        return pkv.paged_prefill_attn_shared(self.q, self.cu, self.k, self.v, self.page_table,
+                                             self.seq_lens, self.x.scale, self.x.max_q_len,
+                                             to_dev(gs), to_dev(gl), max_group,
+                                             dev_status=self.status, **kw)
+
     def dev_status(self):
         torch.cuda.synchronize()
         return int(self.status.item())
