@@ -405,9 +405,7 @@ def prefill_ms(x, dev, stream, reps, warmup, shared=False):
         gsd, gld = to_dev(gs, dev), to_dev(x.meta["prefix_len"], dev)
         cu64 = x.cu_seqlens_q.astype("int64")
         max_group = int(max(cu64[gs[g + 1]] - cu64[gs[g]] for g in range(len(gs) - 1)))
-        pws = pkv.prefill_shared_workspace(x.Tq, x.Hq, x.d, dev)
-    else:
-        pws = pkv.prefill_workspace(dev)
+    pws = pkv.prefill_workspace(dev)
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     times = []
     with torch.cuda.stream(stream):

@@ -87,11 +87,11 @@ typedef enum pkv_status {
 #define PKV_DEV_BAD_WORKSPACE 32  /* prefill: the workspace counters were not zero when the
                                      call started (never cleared, or in use by another call
                                      at the same time); work may have been skipped */
-#define PKV_DEV_BAD_SHARED 64  /* shared-prefix prefill: a prefix group out of range, a
-                                  shared length that is negative, not a whole number of
-                                  pages or longer than a member's cached prefix (that
-                                  request's rows written as NaN), or a member whose
-                                  page-table row does not list the group's shared pages */
+#define PKV_DEV_BAD_SHARED 64  /* shared-prefix prefill: groups that do not partition the
+                                  batch in order, a shared length that is negative, not a
+                                  whole number of pages or longer than a member's cached
+                                  prefix (the rows concerned written as NaN), or a member
+                                  whose page-table row does not list the shared pages */
 
 /* Human-readable name of a pkv_status value. */
 const char *pkv_status_string(int status);
@@ -263,20 +263,20 @@ size_t pkv_prefill_workspace_size(void);
  *
  * The result is that of pkv_paged_prefill_attn on the same arguments (every
  * new token attends keys 0 .. c_r + i of its own request); only the order of
- * work differs.  The call runs two passes of the prefill kernel on `stream`:
- *   1. for each group, the new tokens of all its requests, packed back to
- *      back, against the group's shared keys (no mask: every new token comes
- *      after the prefix), so each shared K/V tile is loaded once per 256
- *      packed query rows rather than once per request; each row's fp32 state
- *      goes to the workspace;
- *   2. each request's new tokens against its keys after the shared prefix,
- *      causally, merged with the row's first-pass state by log-sum-exp.
+ * work differs.  A work item is a block of a group's new tokens, packed back
+ * to back across the group's requests: it runs over the group's shared keys
+ * once for all its rows (no mask: every new token comes after the prefix),
+ * then over each of its requests' own keys from the shared length on, that
+ * request's rows causal and the others masked, with one online softmax per
+ * row over both ranges.  So each shared K/V tile is loaded once per 256
+ * packed query rows rather than once per request, and short requests no
+ * longer leave their query tiles mostly empty.
  *
- *   prefix_group_start  [num_prefix_groups + 1] int32, non-decreasing, within
- *                 [0, batch]: group g is requests prefix_group_start[g] ..
- *                 prefix_group_start[g+1]-1 (consecutive, so their new tokens
- *                 are one contiguous range of q); requests in no group attend
- *                 as in pkv_paged_prefill_attn
+ *   prefix_group_start  [num_prefix_groups + 1] int32: group g is requests
+ *                 prefix_group_start[g] .. prefix_group_start[g+1]-1; the
+ *                 groups partition the batch in order (first entry 0, last
+ *                 entry batch, strictly increasing); a request that shares
+ *                 nothing is a group of one with prefix_len 0
  *   prefix_len    [num_prefix_groups] int32: keys 0 .. prefix_len[g]-1 are
  *                 shared by the group's requests: a whole number of pages,
  *                 listed first in each member's page-table row (the first
@@ -284,15 +284,9 @@ size_t pkv_prefill_workspace_size(void);
  *                 cached prefix.  0 = nothing shared.
  *   num_prefix_groups  groups; 0 makes the call pkv_paged_prefill_attn
  *   max_group_tokens   host upper bound on the new tokens of any one group
- *                 (sizes the first pass's grid); 0 makes the call
- *                 pkv_paged_prefill_attn
- *   workspace     device buffer of at least
- *                 pkv_prefill_shared_workspace_size(total_q_tokens,
- *                 num_q_heads, head_dim) bytes, 16-byte aligned; its first
- *                 pkv_prefill_workspace_size() bytes are the work-queue
- *                 counters, with the same zero-fill contract as for
- *                 pkv_paged_prefill_attn; the rest holds the first pass's row
- *                 states (no initial contents needed)
+ *                 (sizes the grid); 0 makes the call pkv_paged_prefill_attn
+ *   workspace     as for pkv_paged_prefill_attn (pkv_prefill_workspace_size()
+ *                 bytes of work-queue counters, zero-filled once)
  * Other arguments as for pkv_paged_prefill_attn.  Device-detected errors add
  * PKV_DEV_BAD_SHARED (see above) to those of pkv_paged_prefill_attn.
  */
@@ -308,11 +302,6 @@ pkv_status pkv_paged_prefill_attn_shared(const pkv_bf16 *q, const int32_t *cu_se
                                          int max_group_tokens, void *workspace,
                                          size_t workspace_bytes, int32_t *dev_status,
                                          pkv_bf16 *out, void *stream);
-
-/* Bytes of device workspace pkv_paged_prefill_attn_shared needs: the work-queue
- * counters plus (head_dim + 2) fp32 per (new token, query head); 0 for
- * invalid arguments. */
-size_t pkv_prefill_shared_workspace_size(int64_t total_q_tokens, int num_q_heads, int head_dim);
 
 /*
  * Size of the fixed scratch area that pkv_paged_decode_attn_noalloc uses in

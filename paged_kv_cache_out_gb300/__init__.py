@@ -20,6 +20,5 @@ from .binding import (  # noqa: F401
     paged_decode_attn_store,
     paged_prefill_attn,
     paged_prefill_attn_shared,
-    prefill_shared_workspace,
     prefill_workspace,
 )

@@ -40,7 +40,6 @@ SIGNATURES = {
     "pkv_paged_prefill_attn_shared": ([_P, _P, _P, _P, _P, _I64, _P, _I32, _I64, _I32, _I32, _I32,
                                        _I32, _I32, _I64, _F32, _P, _P, _I32, _I32, _P, _SZ, _P, _P,
                                        _P], _I32),
-    "pkv_prefill_shared_workspace_size": ([_I64, _I32, _I32], _SZ),
     "pkv_paged_decode_attn_noalloc": ([_P, _P, _P, _P, _I64, _P, _I32, _I32, _I32, _I32, _I32,
                                        _I64, _F32, _P, _P, _P], _I32),
 }
@@ -203,13 +202,6 @@ def paged_prefill_attn(q, cu_seqlens_q, k_cache, v_cache, page_table, seq_lens, 
     return out
 
 
-def prefill_shared_workspace(total_q_tokens, num_q_heads, head_dim, device=None):
-    """A workspace for paged_prefill_attn_shared (its queue counters zeroed)."""
-    n = int(load_library().pkv_prefill_shared_workspace_size(int(total_q_tokens), int(num_q_heads),
-                                                             int(head_dim)))
-    return torch.zeros(max(n, 16), dtype=torch.uint8, device=device or "cuda")
-
-
 def paged_prefill_attn_shared(q, cu_seqlens_q, k_cache, v_cache, page_table, seq_lens,
                               softmax_scale, max_q_len, prefix_group_start, prefix_len,
                               max_group_tokens, workspace=None, dev_status=None, out=None,
@@ -217,10 +209,12 @@ def paged_prefill_attn_shared(q, cu_seqlens_q, k_cache, v_cache, page_table, seq
     """Ragged causal prefill for requests that share cached prefixes.
 
     prefix_group_start [n_groups + 1] int32: group g is requests
-    prefix_group_start[g] .. prefix_group_start[g+1]-1; prefix_len [n_groups]
-    int32: the keys they share (whole pages, listed first in every member's
-    page-table row).  max_group_tokens bounds the new tokens of any group.
-    The result equals paged_prefill_attn on the same arguments."""
+    prefix_group_start[g] .. prefix_group_start[g+1]-1 (the groups partition
+    the batch in order); prefix_len [n_groups] int32: the keys they share
+    (whole pages, listed first in every member's page-table row; 0 for a
+    request that shares nothing).  max_group_tokens bounds the new tokens of
+    any group.  The result equals paged_prefill_attn on the same arguments.
+    workspace: from prefill_workspace()."""
     _bf16(q, "q"), _bf16(k_cache, "k_cache"), _bf16(v_cache, "v_cache")
     _i32(seq_lens, "seq_lens"), _i32(cu_seqlens_q, "cu_seqlens_q")
     _i32(prefix_group_start, "prefix_group_start"), _i32(prefix_len, "prefix_len")
@@ -236,7 +230,7 @@ def paged_prefill_attn_shared(q, cu_seqlens_q, k_cache, v_cache, page_table, seq
     if out is None:
         out = torch.empty_like(q)
     if workspace is None:
-        workspace = prefill_shared_workspace(Tq, Hq, d, q.device)
+        workspace = prefill_workspace(q.device)
     st = load_library().pkv_paged_prefill_attn_shared(
         _ptr(q), _ptr(cu_seqlens_q), _ptr(k_cache), _ptr(v_cache), _ptr(page_table),
         page_table.stride(0), _ptr(seq_lens), B, Tq, int(max_q_len), Hq, Hkv, d, ps, P,

@@ -168,11 +168,6 @@ __device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
-// Bring one 128-byte line of global memory into L2 (no register, no wait).
-__device__ __forceinline__ void prefetch_l2(const void *p) {
-    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
-}
-
 // Plain bulk copy global -> shared (16-byte aligned addresses, size a multiple of 16).
 // Prefetch one tile of a tensor map into L2 (no shared memory, no barrier).
 __device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap *map, int c0, int c1, int c2) {

@@ -68,19 +68,11 @@ constexpr int kKStages = 2, kVStages = 3;
 constexpr int kProducerWarp = 8, kMmaWarp = 9;  // warps 10 and 11 load K/V tiles with warp 8
 constexpr int kLoaders = 3;              // warps issuing the K/V copies (8, 10, 11)
 constexpr int kItemSlots = 2;            // items published ahead of the consumers
+constexpr int kItemBytes = 128;          // shared memory per published item (>= sizeof(Item))
 constexpr int kItemConsumers = 1 + 8 + (kLoaders - 1);  // MMA, softmax and loader warps
 constexpr int kRankGroups = 256;         // up to this many (token block, request) groups
                                          // are ranked by work in the kernel
 constexpr size_t kWorkspaceBytes = 256;  // queue counters (three used, the rest reserved)
-// The shared-prefix form's workspace: the queue counters, then per (token,
-// query head) row its shared-pass running max and sum, then its unnormalised
-// output row (fp32).
-inline size_t ml_bytes(int64_t tokens, int heads) {
-    return ((static_cast<size_t>(tokens) * heads * 2 * 4 + 255) / 256) * 256;
-}
-inline size_t shared_workspace_bytes(int64_t tokens, int heads, int head_dim) {
-    return kWorkspaceBytes + ml_bytes(tokens, heads) + static_cast<size_t>(tokens) * heads * head_dim * 4;
-}
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kNegBig = -1.0e30f;
 constexpr float kRescaleLog2 = 8.0f;  // lazy rescale threshold (factor 256)
@@ -118,8 +110,8 @@ struct Layout {
     // per query tile: sfull, pfull, odone, ofree; item full/empty[kItemSlots]
     static constexpr int NBARS = 2 + 2 * kKStages + 2 * kVStages + NQ * 4 + 2 * kItemSlots;
     static constexpr int OFF_MISC = OFF_BAR + NBARS * 8;
-    static constexpr int OFF_ITEMS = OFF_MISC + 64;     // decoded items, kItemSlots x 16 ints
-    static constexpr int OFF_RANK = OFF_ITEMS + kItemSlots * 64;  // int order[kRankGroups], weight[kRankGroups]
+    static constexpr int OFF_ITEMS = OFF_MISC + 64;     // decoded items, kItemSlots x kItemBytes
+    static constexpr int OFF_RANK = OFF_ITEMS + kItemSlots * kItemBytes;  // int order[kRankGroups], weight[kRankGroups]
     static constexpr int TOTAL = OFF_RANK + 2 * kRankGroups * 4;
     // at least 116 KB: one block per SM (it holds all 512 TMEM columns)
     static constexpr size_t bytes() { return TOTAL > 118784 ? TOTAL : 118784; }
@@ -149,48 +141,74 @@ __device__ __forceinline__ uint32_t swz_offset(int row, int chunk16, int rows) {
     return static_cast<uint32_t>(blk * rows * 128 + row * 128 + ((c ^ (row & 7)) << 4));
 }
 
-// Passes of the kernel.  kCausal: every request's new tokens against its own
-// keys, causally (the plain prefill).  The two passes of the shared-prefix
-// form split that work for a prefix group (consecutive requests whose first
-// S keys are the same pages):
-//   kShared:  the group's new tokens, packed back to back across its
-//             requests, against the S shared keys; no mask (every new token
-//             comes after the prefix); each row's unnormalised output, running
-//             max and sum go to the workspace;
-//   kPrivate: each request's new tokens against its keys S .. L-1, causally;
-//             the epilogue merges in the row's shared-pass state (log-sum-exp
-//             of the two key ranges) before it normalises and stores.
-enum Mode : int { kCausal = 0, kShared = 1, kPrivate = 2 };
+// Forms of the kernel.  kCausal: each work item is a token block of one
+// request against that request's keys, causally (the plain prefill).
+// kFused (the shared-prefix form): a prefix group is a run of consecutive
+// requests whose first S keys are the same pages; an item is a token block
+// of the group's new tokens, packed back to back across its requests, and
+// its key tiles are first the S shared keys (read once for all the packed
+// rows, no mask: every new token comes after the prefix), then for each
+// request of the block its own keys from S on, with that request's rows
+// causal and the other requests' rows masked.  Each row's online softmax
+// runs over both ranges, so no partial state leaves the block.
+enum Mode : int { kCausal = 0, kFused = 1 };
 
-// The prefix groups of a shared-prefix call (null for kCausal).
+// The prefix groups of a shared-prefix call (unused by kCausal).
 struct Groups {
     const int32_t *start;   // [n + 1]: group g is requests start[g] .. start[g+1]-1
     const int32_t *len;     // [n]: keys shared by the group's requests
     int n;
-    int nreq;               // requests in the call
-    float *part_o;          // [Tq * Hq, D] fp32: shared-pass output rows, unnormalised
-    float *part_ml;         // [Tq * Hq, 2] fp32: their running max (log2 domain) and sum
+    int nreq;               // requests in the call (the groups cover them all)
 };
 
-// Group of request r (start[] is non-decreasing; -1 when r is in none).
-__device__ __forceinline__ int group_of(const Groups &gr, int r) {
-    int lo = 0, hi = gr.n;  // find the last g with start[g] <= r
-    while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (gr.start[mid] <= r) lo = mid; else hi = mid;
-    }
-    return (gr.n > 0 && gr.start[lo] <= r && r < gr.start[lo + 1]) ? lo : -1;
-}
-
-// One work item: query tiles A and B of request r (of prefix group r in the
-// shared pass), token block mt, KV head g; key tiles kt0 .. kt0 + n_kt - 1,
-// keys below klo and above a row's limit masked.
+// One work item: query tiles A and B of token block mt of request r (of
+// prefix group r in kFused), KV head g.  kCausal: key tiles 0 .. n_kt-1.
+// kFused: the ns shared tiles (row of request pr, whose length is L0), then
+// the private tiles of requests rlo .. rhi from klo = S on.
 struct Item {
     int r, g, mt;
     int cu0, n, L, c;
     int tbeg[NQ], tend[NQ], nkt[NQ];
-    int n_kt, kt0, klo, pr;  // pr: the request whose page-table row is read
+    int n_kt, klo, pr;
+    int rlo, rhi, ns, L0;
 };
+static_assert(sizeof(Item) <= kItemBytes, "an item must fit its shared-memory slot");
+
+// A role's position in a kFused item's key tiles: the request whose row
+// holds the current tile (-1 while in the shared tiles), the tile, one past
+// the last tile of its segment, and the number of keys in that row.
+struct Steps {
+    int r, kt, end, L;
+};
+// From request c.r on, the first request of the block with new tokens.
+__device__ __forceinline__ void steps_seek(Steps &c, const Item &it, const int32_t *cu,
+                                           const int32_t *seq_lens) {
+    for (; c.r <= it.rhi; ++c.r) {
+        const int nr = cu[c.r + 1] - cu[c.r];
+        c.L = seq_lens[c.r];
+        c.kt = it.klo / BN;
+        c.end = nr > 0 ? (c.L + BN - 1) / BN : c.kt;
+        if (c.end > c.kt) return;
+    }
+}
+__device__ __forceinline__ void steps_begin(Steps &c, const Item &it, const int32_t *cu,
+                                            const int32_t *seq_lens) {
+    if (it.ns > 0) {
+        c.r = -1;
+        c.kt = 0;
+        c.end = it.ns;
+        c.L = it.L0;
+    } else {
+        c.r = it.rlo;
+        steps_seek(c, it, cu, seq_lens);
+    }
+}
+__device__ __forceinline__ void steps_next(Steps &c, const Item &it, const int32_t *cu,
+                                           const int32_t *seq_lens) {
+    if (++c.kt < c.end) return;
+    c.r = c.r < 0 ? it.rlo : c.r + 1;
+    steps_seek(c, it, cu, seq_lens);
+}
 
 template <int G, int MODE>
 __device__ __forceinline__ void decode_item(int p, int Hkv, int B, int mtiles, const int *order,
@@ -202,44 +220,43 @@ __device__ __forceinline__ void decode_item(int p, int Hkv, int B, int mtiles, c
     const int grp = ranked ? order[grank] : grank;
     it.mt = mtiles - 1 - grp / B;
     it.r = grp % B;
-    it.kt0 = 0;
     it.klo = 0;
     it.pr = it.r;
-    if constexpr (MODE == kShared) {
+    it.ns = 0;
+    if constexpr (MODE == kFused) {
+        // the group's new tokens, packed; its shared keys; the requests of the
+        // token block (rlo .. rhi) and the private tiles are set by the producer
         const int r0 = gr.start[it.r], r1 = gr.start[it.r + 1];
         it.pr = r0;
         it.cu0 = cu_seqlens[r0];
         it.n = cu_seqlens[r1] - it.cu0;
-        it.L = gr.len[it.r];
+        it.klo = gr.len[it.r];
+        it.L = it.klo;
         it.c = 0;
+        it.ns = (it.klo + BN - 1) / BN;
+        it.L0 = seq_lens[r0];
+        it.rlo = r0;
+        it.rhi = r1 - 1;
     } else {
         it.cu0 = cu_seqlens[it.r];
         it.n = cu_seqlens[it.r + 1] - it.cu0;
         it.L = seq_lens[it.r];
         it.c = it.L - it.n;
-        if constexpr (MODE == kPrivate) {
-            const int gi = group_of(gr, it.r);
-            if (gi >= 0) {
-                it.pr = it.r;
-                it.klo = gr.len[gi];
-                it.kt0 = it.klo / BN;
-            }
-        }
     }
     const int blk_tok0 = it.mt * NQ * TOK;
 #pragma unroll
     for (int qt = 0; qt < NQ; ++qt) {
         it.tbeg[qt] = blk_tok0 + qt * TOK;
         it.tend[qt] = min(it.n, it.tbeg[qt] + TOK);
-        const int keys = MODE == kShared ? it.L : it.c + it.tend[qt];
-        it.nkt[qt] = it.tend[qt] > it.tbeg[qt] ? (keys + BN - 1) / BN - it.kt0 : 0;
+        it.nkt[qt] = it.tend[qt] > it.tbeg[qt] ? (it.c + it.tend[qt] + BN - 1) / BN : 0;
     }
     it.n_kt = it.nkt[0] > it.nkt[1] ? it.nkt[0] : it.nkt[1];
 }
 
 // Work of a (token block, request) group in key tiles (a (token block,
-// prefix group) one in the shared pass): 0 for no tokens, 1 for invalid
-// offsets or lengths (the producer only flags those).
+// prefix group) one in kFused, its private tiles estimated from the group's
+// last request): 0 for no tokens, 1 for invalid offsets or lengths (the
+// producer only flags those).
 template <int G, int MODE>
 __device__ __forceinline__ int group_weight(int grp, int B, int mtiles, int64_t Tq, int max_q_len,
                                             int64_t cap, const int32_t *cu_seqlens,
@@ -247,26 +264,21 @@ __device__ __forceinline__ int group_weight(int grp, int B, int mtiles, int64_t 
     constexpr int TOK = BM / G;
     const int mt = mtiles - 1 - grp / B, r = grp % B;
     const int t0 = mt * NQ * TOK;
-    if constexpr (MODE == kShared) {
+    if constexpr (MODE == kFused) {
         const int r0 = gr.start[r], r1 = gr.start[r + 1], S = gr.len[r];
-        if (r0 < 0 || r1 < r0) return 1;
+        if (r0 < 0 || r1 <= r0 || r1 > gr.nreq) return 1;
         const int n = cu_seqlens[r1] - cu_seqlens[r0];
-        if (t0 >= n || S == 0) return 0;
-        if (S < 0 || S > cap) return 1;
-        return (S + BN - 1) / BN;
+        if (t0 >= n) return 0;
+        const int Ll = seq_lens[r1 - 1];
+        if (S < 0 || S > cap || Ll < S || Ll > cap) return 1;
+        return (S + BN - 1) / BN + (Ll + BN - 1) / BN - S / BN;
     } else {
         const int cu0 = cu_seqlens[r], cu1 = cu_seqlens[r + 1];
         const int n = cu1 - cu0, L = seq_lens[r];
         if (cu0 < 0 || n < 0 || cu1 > Tq || (r == 0 && cu0 != 0) || n > max_q_len) return 1;
         if (t0 >= n) return 0;
         if (L - n < 0 || L > cap) return 1;
-        int kt0 = 0;
-        if constexpr (MODE == kPrivate) {
-            const int gi = group_of(gr, r);
-            if (gi >= 0) kt0 = gr.len[gi] / BN;
-        }
-        const int w = (L - n + min(n, t0 + NQ * TOK) + BN - 1) / BN - kt0;
-        return w > 1 ? w : 1;
+        return (L - n + min(n, t0 + NQ * TOK) + BN - 1) / BN;
     }
 }
 
@@ -298,7 +310,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int *taken_s = misc + 6;    // items this block took from the queue (producer)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Lo::OFF_MISC + 32);
     int *order = reinterpret_cast<int *>(smem + Lo::OFF_RANK);
-    Item *items = reinterpret_cast<Item *>(smem + Lo::OFF_ITEMS);  // the published items, decoded
+    // the published items, decoded: slot s at OFF_ITEMS + s * kItemBytes
+    auto item_at = [&](int s) -> Item & { return *reinterpret_cast<Item *>(smem + Lo::OFF_ITEMS + s * kItemBytes); };
     int *weight = order + kRankGroups;
 
     const uint32_t bar0 = smem_u32(smem + Lo::OFF_BAR);
@@ -453,53 +466,89 @@ __global__ void __launch_bounds__(kThreads, 1)
                     first = false;
                     if (q >= n_items) break;
                     if (lane == 0) *taken_s += 1;
-                    if constexpr (MODE == kShared) {
+                    if constexpr (MODE == kFused) {
+                        // the groups must be in range and cover the requests in order
                         const int grp = ranked ? order[q / Hkv] : q / Hkv;
                         const int gi = grp % B;
                         const int r0 = gr.start[gi], r1 = gr.start[gi + 1];
-                        if (r0 < 0 || r1 < r0 || r1 > gr.nreq) {
+                        if (r0 < 0 || r1 <= r0 || r1 > gr.nreq || (gi == 0 && r0 != 0) ||
+                            (gi == B - 1 && r1 != gr.nreq)) {
                             if (lane == 0 && dev_status) atomicOr(dev_status, PKV_DEV_BAD_SHARED);
                             continue;
                         }
                     }
                     decode_item<G, MODE>(q, Hkv, B, mtiles, order, ranked, cu_seqlens, seq_lens, gr, itm);
                     const int cu1 = itm.cu0 + itm.n;
-                    if (itm.cu0 < 0 || itm.n < 0 || cu1 > Tq || (MODE != kShared && itm.r == 0 && itm.cu0 != 0) ||
+                    if (itm.cu0 < 0 || itm.n < 0 || cu1 > Tq || (MODE != kFused && itm.r == 0 && itm.cu0 != 0) ||
                         itm.n > max_q_len) {
                         if (lane == 0 && dev_status) atomicOr(dev_status, PKV_DEV_BAD_CUSEQ);
                         continue;
                     }
                     const int blk_tok0 = itm.mt * NQ * TOK;
                     if (blk_tok0 >= itm.n) continue;
-                    if constexpr (MODE == kShared) {
-                        // the shared keys: a whole number of pages, within the table
-                        if (itm.L == 0) continue;
-                        if (itm.L < 0 || itm.L > cap || (itm.L & ((1 << ps_log2) - 1)) != 0) {
-                            if (lane == 0 && dev_status) atomicOr(dev_status, PKV_DEV_BAD_SHARED);
-                            continue;
-                        }
-                    }
-                    // private pass: the shared keys lie inside the request's
-                    // cached prefix, on the same pages as the group's first
-                    // request (checked once per request)
-                    bool bad_share = false;
-                    if constexpr (MODE == kPrivate) {
-                        if (itm.klo < 0 || itm.klo > itm.c || (itm.klo & ((1 << ps_log2) - 1)) != 0) {
-                            bad_share = true;
-                        } else if (itm.klo > 0 && itm.mt == 0 && itm.g == 0) {
-                            const int gi = group_of(gr, itm.r);
-                            const int32_t *row0 = page_table + (int64_t)gr.start[gi] * pt_stride;
-                            const int32_t *rowr = page_table + (int64_t)itm.r * pt_stride;
-                            bool diff = false;
-                            for (int i = lane; i < (itm.klo >> ps_log2); i += 32) diff |= row0[i] != rowr[i];
+                    const int blk_tok1 = min(itm.n, blk_tok0 + NQ * TOK);
+                    int bad = 0;  // a PKV_DEV_* bit: the block's rows are written as NaN
+                    if constexpr (MODE == kFused) {
+                        // the shared keys: a whole number of pages within the table;
+                        // the requests of the token block, each with the shared keys
+                        // inside its cached prefix and the group's shared pages first
+                        // in its row (checked once per request), and their private tiles
+                        const int S = itm.klo;
+                        if (S < 0 || S > cap || (S & ((1 << ps_log2) - 1)) != 0 || itm.L0 > cap) {
+                            bad = PKV_DEV_BAD_SHARED;
+                        } else {
+                            const int r0 = itm.pr, r1 = itm.rhi + 1;
+                            // the request holding packed token t: the last r with cu[r] <= t
+                            auto find_req = [&](int t) -> int {
+                                int lo = r0, hi = r1;  // cu[lo] <= t < cu[hi]
+                                while (hi - lo > 1) {
+                                    const int step = (hi - lo + 31) / 32;
+                                    const int cand = lo + lane * step;
+                                    const bool le = cand < hi && cu_seqlens[cand] <= t;
+                                    const unsigned m = __ballot_sync(0xffffffffu, le);
+                                    lo += (31 - __clz(m)) * step;
+                                    hi = min(hi, lo + step);
+                                }
+                                return lo;
+                            };
+                            itm.rlo = find_req(itm.cu0 + blk_tok0);
+                            itm.rhi = find_req(itm.cu0 + blk_tok1 - 1);
+                            int tiles = 0;
+                            bool bs = false, bl = false, diff = false;
+                            for (int r = itm.rlo + lane; r <= itm.rhi; r += 32) {
+                                const int c0r = cu_seqlens[r], nr = cu_seqlens[r + 1] - c0r, Lr = seq_lens[r];
+                                if (nr <= 0) continue;
+                                if (Lr - nr < S) bs = true;
+                                if (Lr > cap) bl = true;
+                                if (!bs && !bl) tiles += (Lr + BN - 1) / BN - S / BN;
+                            }
+                            // each member's row lists the shared pages (the item of KV
+                            // head 0 that holds the member's first new token checks)
+                            if (itm.g == 0 && S > 0) {
+                                for (int r = itm.rlo; r <= itm.rhi; ++r) {
+                                    const int c0r = cu_seqlens[r];
+                                    if (r == r0 || c0r < itm.cu0 + blk_tok0 || cu_seqlens[r + 1] == c0r) continue;
+                                    const int32_t *rowr = page_table + (int64_t)r * pt_stride;
+                                    const int32_t *row0 = page_table + (int64_t)r0 * pt_stride;
+                                    for (int i = lane; i < (S >> ps_log2); i += 32) diff |= row0[i] != rowr[i];
+                                }
+                            }
                             if (__any_sync(0xffffffffu, diff) && lane == 0 && dev_status)
                                 atomicOr(dev_status, PKV_DEV_BAD_SHARED);
+                            tiles = __reduce_add_sync(0xffffffffu, tiles);
+                            if (__any_sync(0xffffffffu, bs)) bad = PKV_DEV_BAD_SHARED;
+                            else if (__any_sync(0xffffffffu, bl)) bad = PKV_DEV_BAD_SEQLEN;
+                            itm.n_kt = itm.ns + tiles;
+#pragma unroll
+                            for (int qt = 0; qt < NQ; ++qt)
+                                itm.nkt[qt] = itm.tend[qt] > itm.tbeg[qt] ? itm.n_kt : 0;
+                            if (itm.n_kt == 0) continue;
                         }
+                    } else if (itm.c < 0 || itm.L > cap) {
+                        bad = PKV_DEV_BAD_SEQLEN;
                     }
-                    if (itm.c < 0 || itm.L > cap || bad_share) {
-                        if (lane == 0 && dev_status)
-                            atomicOr(dev_status, bad_share ? PKV_DEV_BAD_SHARED : PKV_DEV_BAD_SEQLEN);
-                        const int blk_tok1 = min(itm.n, blk_tok0 + NQ * TOK);
+                    if (bad) {
+                        if (lane == 0 && dev_status) atomicOr(dev_status, bad);
                         for (int idx = lane; idx < (blk_tok1 - blk_tok0) * G * D; idx += 32) {
                             const int t = blk_tok0 + idx / (G * D);
                             const int rem = idx % (G * D);
@@ -518,42 +567,67 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0) {
                     item_ring[slot] = p;
                     bad_flag[slot] = 0;
-                    if (p >= 0) items[slot] = itm;
+                    if (p >= 0) item_at(slot) = itm;
                     mbar_arrive(BAR(B_IFULL(slot)));
                 }
                 __syncwarp();
             } else {
                 if (!mbar_wait_warp(BAR(B_IFULL(slot)), (ii / kItemSlots) & 1, abort_flag, dev_status)) break;
                 p = item_ring[slot];
-                if (p >= 0) itm = items[slot];
+                if (p >= 0) itm = item_at(slot);
             }
             if (p < 0) break;
 
-            const int32_t *prow = page_table + (int64_t)(MODE == kShared ? itm.pr : itm.r) * pt_stride;
-            const int L = itm.L, g = itm.g, kt0 = MODE == kPrivate ? itm.kt0 : 0;
-            // j below counts the item's key tiles; its keys start at (kt0 + j) BN
-            auto load_ids = [&](int j, int *dstp) {
+            const int32_t *prow = page_table + (int64_t)itm.r * pt_stride;
+            const int L = itm.L, g = itm.g;
+            // kFused: the row, key tile and keys-in-row of the next K and the
+            // next V tile (K tiles come one step ahead of V tiles)
+            Steps ck{}, cv{};
+            if constexpr (MODE == kFused) {
+                steps_begin(ck, itm, cu_seqlens, seq_lens);
+                cv = ck;
+            }
+            // page ids of tile kt's keys lane + 32 r of `row` (Lr keys)
+            auto load_ids = [&](const int32_t *row, int Lr, int kt, int *dstp) {
 #pragma unroll
                 for (int r = 0; r < 4; ++r) {
-                    const int kk = (kt0 + j) * BN + r * 32 + lane;
-                    dstp[r] = kk < L ? prow[kk >> ps_log2] : 0;
+                    const int kk = kt * BN + r * 32 + lane;
+                    dstp[r] = kk < Lr ? row[kk >> ps_log2] : 0;
                 }
             };
-            // page ids in warp-wide windows of 32 page boxes, the next window loaded ahead
-            auto load_window = [&](int w) -> int {
+            // page ids in warp-wide windows of 32 page boxes, the next window
+            // loaded ahead; a new row (kFused moves to another request's row)
+            // reloads both windows
+            auto load_window = [&](const int32_t *row, int Lr, int w) -> int {
                 const int key = (32 * w + lane) * box_rows;
-                return (!SMALL && key < L) ? prow[key >> ps_log2] : 0;
+                return (!SMALL && key < Lr) ? row[key >> ps_log2] : 0;
             };
-            int w_cur = (kt0 * bpt) >> 5;
-            int pg_cur = load_window(w_cur), pg_nxt = load_window(w_cur + 1);
-            // page id of page box pb of tile j (lanes past the tile's boxes get
-            // a neighbour's id, unused)
-            auto page_of = [&](int j, int pb) -> int {
-                const int b0 = (kt0 + j) * bpt;
-                if ((b0 >> 5) != w_cur) {
-                    w_cur = b0 >> 5;
+            const int32_t *win_row = nullptr;
+            int w_cur = 0, pg_cur = 0, pg_nxt = 0;
+            if constexpr (MODE != kFused) {  // one row per item: its first windows at once
+                pg_cur = load_window(prow, L, 0);
+                pg_nxt = load_window(prow, L, 1);
+            }
+            // page id of page box pb of key tile kt of `row` (lanes past the
+            // tile's boxes get a neighbour's id, unused)
+            auto page_of = [&](const int32_t *row, int Lr, int kt, int pb) -> int {
+                const int b0 = kt * bpt;
+                const int w = b0 >> 5;
+                if constexpr (MODE == kFused) {
+                    if (row != win_row || w < w_cur || w > w_cur + 1) {
+                        win_row = row;
+                        w_cur = w;
+                        pg_cur = load_window(row, Lr, w);
+                        pg_nxt = load_window(row, Lr, w + 1);
+                    } else if (w == w_cur + 1) {
+                        w_cur = w;
+                        pg_cur = pg_nxt;
+                        pg_nxt = load_window(row, Lr, w + 1);
+                    }
+                } else if (w != w_cur) {  // tiles come in order: the next window
+                    w_cur = w;
                     pg_cur = pg_nxt;
-                    pg_nxt = load_window(w_cur + 1);
+                    pg_nxt = load_window(row, Lr, w + 1);
                 }
                 return __shfl_sync(0xffffffffu, pg_cur, (b0 + min(pb, bpt - 1)) & 31);
             };
@@ -566,15 +640,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t full = BAR(kv ? B_VFULL(s) : B_KFULL(s));
                 const uint32_t empty = BAR(kv ? B_VEMPTY(s) : B_KEMPTY(s));
                 const uint32_t dst = (kv ? sV : sK) + s * Lo::KV_BYTES;
-                const int key0 = (kt0 + j) * BN;
-                const int nkeys = min(BN, L - key0);  // keys of this tile that exist in pages
+                // the tile's row, key tile and the keys of that row
+                const int32_t *trow = prow;
+                int tkt = j, tL = L;
+                if constexpr (MODE == kFused) {
+                    const Steps &c = kv ? cv : ck;
+                    trow = page_table + (int64_t)(c.r < 0 ? itm.pr : c.r) * pt_stride;
+                    tkt = c.kt;
+                    tL = c.L;
+                }
+                const int key0 = tkt * BN;
+                const int nkeys = min(BN, tL - key0);  // keys of this tile that exist in pages
                 if (t >= static_cast<uint32_t>(ns) && !mbar_wait_warp(empty, ph ^ 1, abort_flag, dev_status))
                     return false;
                 if constexpr (!SMALL) {
                     const int nbox = (nkeys + box_rows - 1) / box_rows;  // page boxes, <= 16
                     const int b = li + kLoaders * lane;                  // this lane's box
                     const int pb = b / NBLK, blk = b % NBLK;
-                    const int pg = page_of(j, pb);
+                    const int pg = page_of(trow, tL, tkt, pb);
                     const bool mine = pb < nbox;
                     // a page id outside the pool is flagged; its box is read from
                     // a row before the pool, which the copy engine fills with zeros
@@ -605,15 +688,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // page ids of this tile's keys: loaded for K(j) (or
                     // prefetched while V(j-1) was issued) and reused for V(j),
                     // which prefetches those of tile j + 1
-                    if (kv == 0) {
+                    if constexpr (MODE == kFused) {
+                        // (the tile's row may change between tiles: no lookahead)
+                        if (kv == 0) load_ids(trow, tL, tkt, gpg);
+                    } else if (kv == 0) {
                         if (j == 0) {
-                            load_ids(0, gpg);
+                            load_ids(prow, L, 0, gpg);
                         } else {
 #pragma unroll
                             for (int r = 0; r < 4; ++r) gpg[r] = gpg_next[r];
                         }
                     } else if (j + 1 < itm.n_kt) {
-                        load_ids(j + 1, gpg_next);
+                        load_ids(prow, L, j + 1, gpg_next);
                     }
                     bool bad = false;
 #pragma unroll
@@ -638,6 +724,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     flush_gather(true);
                     gather_pending = full;
                 }
+                if constexpr (MODE == kFused) steps_next(kv ? cv : ck, itm, cu_seqlens, seq_lens);
                 return true;
             };
             // K(0) first: it needs only a free K slot; the Q tiles wait until
@@ -667,8 +754,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                             tma_prefetch_3d(&qmap, blk * 64, g * G, itm.cu0 + itm.tbeg[qt]);
                 }
                 if (!SMALL) {
-                    const int nbox0 = (min(BN, L - kt0 * BN) + box_rows - 1) / box_rows;
-                    const int pg0 = page_of(0, lane);
+                    const int32_t *row0 = MODE == kFused ? page_table + (int64_t)(ck.r < 0 ? itm.pr : ck.r) * pt_stride
+                                                         : prow;
+                    const int kt0 = MODE == kFused ? ck.kt : 0, L0 = MODE == kFused ? ck.L : L;
+                    const int nbox0 = (min(BN, L0 - kt0 * BN) + box_rows - 1) / box_rows;
+                    const int pg0 = page_of(row0, L0, kt0, lane);
                     if (lane < nbox0 && pg0 >= 0 && pg0 < num_pages) {
                         const int row = (pg0 << ps_log2) + ((kt0 * BN + lane * box_rows) & ps_mask);
 #pragma unroll
@@ -740,9 +830,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!mbar_wait_warp(BAR(B_IFULL(slot)), (ii / kItemSlots) & 1, abort_flag, dev_status)) break;
             const int p = item_ring[slot];
             if (p < 0) break;
-            const Item &itm = items[slot];
+            const Item &itm = item_at(slot);
             const int nk[NQ] = {itm.nkt[0], itm.nkt[1]};
             const int n_kt = itm.n_kt, L = itm.L;
+            Steps cm{};  // kFused: the row and keys of each V tile
+            if constexpr (MODE == kFused) steps_begin(cm, itm, cu_seqlens, seq_lens);
             ok = mbar_wait_warp(BAR(B_QFULL), ii & 1, abort_flag, dev_status) &&
                  mbar_wait_warp(BAR(B_KFULL(kt % kKStages)), (kt / kKStages) & 1, abort_flag, dev_status);
             if (!ok) break;
@@ -759,12 +851,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ok = false;
                     break;
                 }
-                const int kt0 = MODE == kPrivate ? itm.kt0 : 0;
-                if (j == n_kt - 1 && (kt0 + j + 1) * BN > L) {
-                    // keys past the sequence end hold stale pool data (maybe NaN):
-                    // zero those V rows so that P = 0 there contributes exactly 0
+                const int tkt = MODE == kFused ? cm.kt : j, tL = MODE == kFused ? cm.L : L;
+                if constexpr (MODE == kFused) steps_next(cm, itm, cu_seqlens, seq_lens);
+                if ((tkt + 1) * BN > tL) {
+                    // keys past the end of the tile's row hold stale pool data
+                    // (maybe NaN): zero those V rows so that P = 0 there
+                    // contributes exactly 0
                     const uint32_t vb = sV + s * Lo::KV_BYTES;
-                    const int first_dead = L - (kt0 + j) * BN;
+                    const int first_dead = tL - tkt * BN;
                     for (int idx = lane; idx < (BN - first_dead) * (D / 8); idx += 32) {
                         const int key = first_dead + idx / (D / 8), ch = idx % (D / 8);
                         *reinterpret_cast<uint4 *>(smem + (vb - smem_u32(smem)) +
@@ -843,25 +937,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!mbar_wait_warp(BAR(B_IFULL(slot)), (ii / kItemSlots) & 1, abort_flag, dev_status)) break;
             const int p = item_ring[slot];
             if (p < 0) break;
-            const Item &itm = items[slot];
+            const Item &itm = item_at(slot);
             const int tok = (qt ? itm.tbeg[1] : itm.tbeg[0]) + row / G;
             const bool row_valid = tok < (qt ? itm.tend[1] : itm.tend[0]);
             const bool warp_live = __any_sync(0xffffffffu, row_valid);
-            // last key this row may see: its own position, or in the shared
-            // pass the last shared key
-            const int lim = MODE == kShared ? itm.L - 1 : itm.c + tok;
+            const int lim = itm.c + tok;  // kCausal: the last key this row may see
+            // kFused: the row's request and the last of its keys it may see;
+            // the step cursor tells whose keys each tile holds
+            int r_row = -1, lim_row = 0;
+            Steps cs{};
+            if constexpr (MODE == kFused) {
+                if (row_valid) {
+                    const int t = itm.cu0 + tok;
+                    int r = itm.rlo;
+                    while (r < itm.rhi && cu_seqlens[r + 1] <= t) ++r;
+                    r_row = r;
+                    lim_row = seq_lens[r] - cu_seqlens[r + 1] + t;
+                }
+                steps_begin(cs, itm, cu_seqlens, seq_lens);
+            }
             const int my_kt = (qt ? itm.nkt[1] : itm.nkt[0]);
             float m_ref = kNegBig, l_sum = 0.f;
-            if constexpr (MODE == kPrivate) {
-                // the row's shared-pass state, read by the epilogue: into L2 now
-                if (itm.klo > 0 && row_valid) {
-                    const int64_t hrow = (int64_t)(itm.cu0 + tok) * Hq + (int64_t)itm.g * G + row % G;
-                    const char *po = reinterpret_cast<const char *>(gr.part_o + hrow * D);
-#pragma unroll
-                    for (int b = 0; b < D * 4 / 128; ++b) prefetch_l2(po + 128 * b);
-                    prefetch_l2(gr.part_ml + 2 * hrow);
-                }
-            }
             // tcgen05.ld/st are warp-collective: every wait outcome is warp-uniform
             for (int j = 0; j < my_kt; ++j) {
                 // S(j) complete implies PV(j-1) complete: O is stable and P free
@@ -881,10 +977,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // used (their output is not stored, and each row of P only
                     // feeds the same row of O), so a warp holding such rows does
                     // not pay for masking on every tile.
-                    const int key0 = ((MODE == kPrivate ? itm.kt0 : 0) + j) * BN;
-                    const int nvalid = row_valid ? lim - key0 + 1 : BN;  // keys kept in this row
-                    // private pass: the shared keys below klo are the shared pass's
-                    const int nlow = MODE == kPrivate ? itm.klo - key0 : 0;  // keys dropped below
+                    // nvalid: keys of the tile this row keeps from the start;
+                    // nlow: kFused private tiles drop the shared keys below klo
+                    int key0 = j * BN, nvalid = row_valid ? lim - key0 + 1 : BN, nlow = 0;
+                    if constexpr (MODE == kFused) {
+                        key0 = cs.kt * BN;
+                        if (cs.r < 0) {  // shared keys: every row, no causal limit
+                            nvalid = row_valid ? itm.klo - key0 : BN;
+                        } else {         // request cs.r's own keys: its rows only
+                            nvalid = row_valid ? (r_row == cs.r ? lim_row - key0 + 1 : 0) : BN;
+                            nlow = itm.klo - key0;
+                        }
+                    }
                     if (__any_sync(0xffffffffu, nvalid < BN || nlow > 0)) {
 #pragma unroll
                         for (int i = 0; i < BN; ++i)
@@ -943,6 +1047,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     tmem_wait_st();  // P and O stores
                 }
+                if constexpr (MODE == kFused) steps_next(cs, itm, cu_seqlens, seq_lens);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(BAR(B_PFULL(qt)));
@@ -953,80 +1058,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ++od;
                 if (!ok) break;
                 tc_fence_after();
+                // the output row out of tensor memory 32 columns at a time,
+                // normalised, packed to bf16 and stored by its own thread in
+                // 32-byte pieces (whole sectors)
                 const bool poison = (bad_flag[slot] != 0) || (*abort_flag != 0);
-                const int64_t hrow = (int64_t)(itm.cu0 + tok) * Hq + (int64_t)itm.g * G + row % G;
-                if constexpr (MODE == kShared) {
-                    // the row's state goes to the workspace for the private pass:
-                    // the output row unnormalised, the running max and sum (a
-                    // poisoned row's sum is NaN, which carries into its output)
-                    if (warp_live) {
+                const float inv = row_valid ? 1.f / l_sum : 0.f;
+                const int64_t out_row = ((int64_t)(itm.cu0 + tok) * Hq + (int64_t)itm.g * G + row % G) * D;
+                if (warp_live) {
 #pragma unroll
-                        for (int cc = 0; cc < D / 32; ++cc) {
-                            uint32_t ov[32];
-                            tmem_ld_32cols(tm_o(qt) + lane_off + cc * 32, ov);
-                            tmem_wait_ld();
-                            if (row_valid) {
-                                float4 *dst = reinterpret_cast<float4 *>(gr.part_o + hrow * D + cc * 32);
+                    for (int cc = 0; cc < D / 32; ++cc) {
+                        uint32_t ov[32];
+                        tmem_ld_32cols(tm_o(qt) + lane_off + cc * 32, ov);
+                        tmem_wait_ld();
+                        uint32_t pk[16];
 #pragma unroll
-                                for (int e = 0; e < 8; ++e)
-                                    dst[e] = make_float4(__uint_as_float(ov[4 * e]), __uint_as_float(ov[4 * e + 1]),
-                                                         __uint_as_float(ov[4 * e + 2]),
-                                                         __uint_as_float(ov[4 * e + 3]));
-                            }
-                        }
-                    }
-                    if (row_valid) {
-                        gr.part_ml[2 * hrow] = m_ref;
-                        gr.part_ml[2 * hrow + 1] = poison ? __int_as_float(0x7fc00000) : l_sum;
-                    }
-                } else {
-                    // the output row out of tensor memory 32 columns at a time,
-                    // normalised, packed to bf16 and stored by its own thread in
-                    // 32-byte pieces (whole sectors).  In the private pass the
-                    // shared pass's state of the row is folded in first: both
-                    // are relative to their own running max (log2 domain), so
-                    // each is weighted by 2^(its max - the larger max).
-                    float w_own = 1.f, w_sh = 0.f, denom = l_sum;
-                    const float4 *osh = nullptr;
-                    if (MODE == kPrivate && itm.klo > 0 && row_valid) {
-                        const float m1 = __ldg(gr.part_ml + 2 * hrow), l1 = __ldg(gr.part_ml + 2 * hrow + 1);
-                        const float mx = fmaxf(m1, m_ref);
-                        w_sh = ex2(m1 - mx);
-                        w_own = ex2(m_ref - mx);
-                        denom = l1 * w_sh + l_sum * w_own;
-                        osh = reinterpret_cast<const float4 *>(gr.part_o + hrow * D);
-                    }
-                    const float inv = row_valid ? 1.f / denom : 0.f;
-                    const float c_own = w_own * inv, c_sh = w_sh * inv;
-                    const int64_t out_row = hrow * D;
-                    if (warp_live) {
-#pragma unroll
-                        for (int cc = 0; cc < D / 32; ++cc) {
-                            uint32_t ov[32];
-                            tmem_ld_32cols(tm_o(qt) + lane_off + cc * 32, ov);
-                            tmem_wait_ld();
-                            float o[32];
-#pragma unroll
-                            for (int e = 0; e < 32; ++e) o[e] = __uint_as_float(ov[e]) * c_own;
-                            if (osh) {
-#pragma unroll
-                                for (int e = 0; e < 8; ++e) {
-                                    const float4 v = __ldg(osh + cc * 8 + e);
-                                    o[4 * e] += v.x * c_sh;
-                                    o[4 * e + 1] += v.y * c_sh;
-                                    o[4 * e + 2] += v.z * c_sh;
-                                    o[4 * e + 3] += v.w * c_sh;
-                                }
-                            }
-                            uint32_t pk[16];
-#pragma unroll
-                            for (int e = 0; e < 32; e += 2)
-                                pk[e / 2] = poison ? 0x7fc07fc0u  // two bf16 NaNs
-                                                   : pack_bf16x2(o[e], o[e + 1]);
-                            if (row_valid) {
-                                st_global_32B(out + out_row + cc * 32, pk);
-                                st_global_32B(out + out_row + cc * 32 + 16, pk + 8);
-                            }
+                        for (int e = 0; e < 32; e += 2)
+                            pk[e / 2] = poison ? 0x7fc07fc0u  // two bf16 NaNs
+                                               : pack_bf16x2(__uint_as_float(ov[e]) * inv,
+                                                             __uint_as_float(ov[e + 1]) * inv);
+                        if (row_valid) {
+                            st_global_32B(out + out_row + cc * 32, pk);
+                            st_global_32B(out + out_row + cc * 32 + 16, pk + 8);
                         }
                     }
                 }
@@ -1158,20 +1210,12 @@ static pkv_status prefill_entry(const pkv_bf16 *q, const int32_t *cu_seqlens_q, 
     if (!pkv_host::aligned16(q) || !pkv_host::aligned16(k_cache) || !pkv_host::aligned16(v_cache) ||
         !pkv_host::aligned16(out) || !pkv_host::aligned16(workspace))
         return PKV_EINVAL;
-    const size_t need = shared ? shared_workspace_bytes(total_q_tokens, num_q_heads, head_dim)
-                               : kWorkspaceBytes;
-    if (workspace_bytes < need) return PKV_EINVAL;
+    if (workspace_bytes < kWorkspaceBytes) return PKV_EINVAL;
     if (num_pages * page_size > 0x7fffffffll || total_q_tokens > 0x7fffffffll)
         return PKV_EUNSUPPORTED;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     unsigned int *sched = static_cast<unsigned int *>(workspace);
-    Groups gr{group_start, group_len, shared ? num_groups : 0, batch, nullptr, nullptr};
-    if (shared) {
-        uint8_t *w = static_cast<uint8_t *>(workspace);
-        const size_t ml = ml_bytes(total_q_tokens, num_q_heads);
-        gr.part_ml = reinterpret_cast<float *>(w + kWorkspaceBytes);
-        gr.part_o = reinterpret_cast<float *>(w + kWorkspaceBytes + ml);
-    }
+    const Groups gr{group_start, group_len, shared ? num_groups : 0, batch};
 #define PKV_PREFILL_CASE(DD, GG)                                                                      \
     if (head_dim == DD && G == GG) {                                                                  \
         if (!shared)                                                                                  \
@@ -1179,16 +1223,10 @@ static pkv_status prefill_entry(const pkv_bf16 *q, const int32_t *cu_seqlens_q, 
                                            page_table_stride, seq_lens, batch, total_q_tokens,         \
                                            max_q_len, num_kv_heads, page_size, num_pages,              \
                                            softmax_scale, gr, sched, dev_status, out, st);            \
-        pkv_status r1 = launch<DD, GG, kShared>(q, cu_seqlens_q, k_cache, v_cache, page_table,        \
-                                                page_table_stride, seq_lens, num_groups,              \
-                                                total_q_tokens, max_group_tokens, num_kv_heads,       \
-                                                page_size, num_pages, softmax_scale, gr, sched,       \
-                                                dev_status, out, st);                                 \
-        if (r1 != PKV_OK) return r1;                                                                  \
-        return launch<DD, GG, kPrivate>(q, cu_seqlens_q, k_cache, v_cache, page_table,                 \
-                                        page_table_stride, seq_lens, batch, total_q_tokens,            \
-                                        max_q_len, num_kv_heads, page_size, num_pages, softmax_scale,  \
-                                        gr, sched, dev_status, out, st);                              \
+        return launch<DD, GG, kFused>(q, cu_seqlens_q, k_cache, v_cache, page_table,                   \
+                                      page_table_stride, seq_lens, num_groups, total_q_tokens,         \
+                                      max_group_tokens, num_kv_heads, page_size, num_pages,            \
+                                      softmax_scale, gr, sched, dev_status, out, st);                 \
     }
     PKV_PREFILL_CASE(128, 1)
     PKV_PREFILL_CASE(128, 2)
@@ -1206,11 +1244,6 @@ static pkv_status prefill_entry(const pkv_bf16 *q, const int32_t *cu_seqlens_q, 
 }  // namespace pkv
 
 extern "C" size_t pkv_prefill_workspace_size(void) { return pkv::prefill::kWorkspaceBytes; }
-
-extern "C" size_t pkv_prefill_shared_workspace_size(int64_t total_q_tokens, int num_q_heads, int head_dim) {
-    if (total_q_tokens < 0 || num_q_heads <= 0 || head_dim <= 0) return 0;
-    return pkv::prefill::shared_workspace_bytes(total_q_tokens, num_q_heads, head_dim);
-}
 
 extern "C" pkv_status pkv_paged_prefill_attn(const pkv_bf16 *q, const int32_t *cu_seqlens_q,
                                              const pkv_bf16 *k_cache, const pkv_bf16 *v_cache,

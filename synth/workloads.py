@@ -306,22 +306,25 @@ def share_prefix(x: PagedInputs, groups) -> PagedInputs:
     sequences).  ``shared_tokens`` must be a whole number of pages within
     every member's cached prefix, so the new tokens' slots are untouched.
     The pages the members held before stay in the pool, unreferenced.  The
-    groups are recorded in ``x.meta`` as ``prefix_group_start`` ([n + 1]) and
-    ``prefix_len`` ([n]) int32 arrays.
+    groups, with every request outside them as a group of one sharing
+    nothing, are recorded in ``x.meta`` as ``prefix_group_start`` ([n + 1],
+    a partition of the batch) and ``prefix_len`` ([n]) int32 arrays.
     """
     ps = x.page_size
     pt = x.page_table.copy()
-    starts, lens = [], []
-    for first, end, shared in groups:
-        assert shared % ps == 0 and first < end
+    starts, lens = [0], []
+    for first, end, shared in sorted(groups):
+        assert shared % ps == 0 and first < end and first >= starts[-1]
         assert (x.prefix_lens[first:end] >= shared).all()
         pt[first + 1:end, :shared // ps] = pt[first, :shared // ps]
-        if starts and starts[-1] != first:
-            raise ValueError("groups must be consecutive and in request order")
-        if not starts:
-            starts.append(first)
+        for r in range(starts[-1], first):  # requests before the group share nothing
+            starts.append(r + 1)
+            lens.append(0)
         starts.append(end)
         lens.append(shared)
+    for r in range(starts[-1], x.B):
+        starts.append(r + 1)
+        lens.append(0)
     x.page_table = pt
     x.meta["prefix_group_start"] = np.asarray(starts, dtype=np.int32)
     x.meta["prefix_len"] = np.asarray(lens, dtype=np.int32)

@@ -114,10 +114,8 @@ def test_prefill_rejects_bad_arguments(lib):
 def _prefill_shared(lib, **kw):
     a = dict(q=FAKE, cu=FAKE, k=FAKE, v=FAKE, pt=FAKE, stride=4, sl=FAKE, B=2, Tq=10, maxq=8,
              Hq=16, Hkv=8, d=128, ps=16, P=64, scale=0.088, gs=FAKE, gl=FAKE, ng=1, maxg=10,
-             ws=FAKE, ws_bytes=None, status=NULL, out=FAKE, stream=NULL)
+             ws=FAKE, ws_bytes=256, status=NULL, out=FAKE, stream=NULL)
     a.update(kw)
-    if a["ws_bytes"] is None:
-        a["ws_bytes"] = lib.pkv_prefill_shared_workspace_size(a["Tq"], a["Hq"], a["d"])
     return lib.pkv_paged_prefill_attn_shared(
         a["q"], a["cu"], a["k"], a["v"], a["pt"], a["stride"], a["sl"], a["B"], a["Tq"], a["maxq"],
         a["Hq"], a["Hkv"], a["d"], a["ps"], a["P"], a["scale"], a["gs"], a["gl"], a["ng"], a["maxg"],
@@ -126,24 +124,21 @@ def _prefill_shared(lib, **kw):
 
 def test_prefill_shared_rejects_bad_arguments(lib):
     """The shared-prefix entry point runs the prefill checks, plus its own:
-    group arrays present when there are groups, counts not negative, and a
-    workspace large enough for the first pass's row states."""
+    group arrays present when there are groups, counts not negative."""
     E, U = pkv.binding.EINVAL, pkv.binding.EUNSUPPORTED
-    need = lib.pkv_prefill_shared_workspace_size(10, 16, 128)
-    assert need == lib.pkv_prefill_workspace_size() + 1280 + 10 * 16 * 128 * 4  # counters, (m, l), rows
-    assert lib.pkv_prefill_shared_workspace_size(-1, 16, 128) == 0
     assert _prefill_shared(lib, cu=NULL) == E
     assert _prefill_shared(lib, gs=NULL) == E
     assert _prefill_shared(lib, gl=NULL) == E
     assert _prefill_shared(lib, ng=-1) == E
     assert _prefill_shared(lib, maxg=-1) == E
-    assert _prefill_shared(lib, ws_bytes=need - 16) == E     # no room for the row states
+    assert _prefill_shared(lib, ws_bytes=8) == E            # workspace too small
+    assert _prefill_shared(lib, ws=ctypes.c_void_p(0x10008)) == E   # misaligned workspace
     assert _prefill_shared(lib, d=256) == U
     assert _prefill_shared(lib, ps=3) == U
     assert _prefill_shared(lib, Tq=0) == 0
-    # no groups: the plain prefill's workspace is enough, null group arrays allowed
-    assert _prefill_shared(lib, ng=0, gs=NULL, gl=NULL, ws_bytes=8) == E
+    # no groups: the plain prefill's checks, null group arrays allowed
     assert _prefill_shared(lib, ng=0, gs=NULL, gl=NULL, cu=NULL) == E
+    assert _prefill_shared(lib, maxg=0, gs=NULL, gl=NULL, ws_bytes=8) == E
 
 
 def test_workspace_size_is_zero_for_bad_sizes(lib):

@@ -56,8 +56,9 @@ def _groups_case(seed, d, G, ps, new_lens, prefix_lens, groups):
 
 
 # shared lengths: whole pages, not always whole 128-key tiles; groups of one,
-# several and no shared keys; a request in no group; groups whose packed new
-# tokens span several 128-row query tiles
+# several and no shared keys; a request in no group (a group of one sharing
+# nothing); groups whose packed new tokens span several 128-row query tiles
+# and token blocks that span several requests
 CASES = [
     # d, G, ps, new_lens, prefix_lens, groups (first, end, shared tokens)
     (128, 2, 16, [100, 60, 200, 33, 70, 90], [320, 400, 320, 160, 208, 50],
@@ -96,6 +97,21 @@ def test_no_groups_is_the_plain_prefill_bit_for_bit():
     assert (plain.view(torch.int16) == got.view(torch.int16)).all()
 
 
+def test_many_short_requests_in_one_group():
+    """Requests of 1-9 new tokens: one 128-row tile holds many requests, each
+    with its own private key tiles; requests with no new tokens in between."""
+    rng = np.random.default_rng(7)
+    n = rng.integers(0, 10, size=40)
+    n[0] = 3
+    x = make_inputs(seed=101, Hq=16, Hkv=8, d=128, page_size=16, new_lens=n,
+                    prefix_lens=np.full(40, 272))
+    x = share_prefix(x, [(0, 40, 256)])
+    r = Run(x).store()
+    got = r.prefill_shared()
+    assert r.dev_status() == 0
+    assert max_err(as_f64(got), oracle.run_inputs(x)) <= TOL
+
+
 def test_shared_prefix_workload_sampled_rows():
     x = make_config("shared_prefix_prefill", seed=1)
     r = Run(x).store()
@@ -112,6 +128,11 @@ def test_bad_shared_length_and_mismatched_pages_are_reported():
     x = _groups_case(98, 128, 2, 16, [20, 30], [64, 64], [(0, 2, 64)])
     r = Run(x).store()
     r.prefill_shared(prefix_len=[40])
+    assert r.dev_status() & pkv.DEV_BAD_SHARED
+    # groups that do not partition the batch
+    x = _groups_case(98, 128, 2, 16, [20, 30], [64, 64], [(0, 2, 64)])
+    r = Run(x).store()
+    r.prefill_shared(group_start=[0, 1], prefix_len=[64])
     assert r.dev_status() & pkv.DEV_BAD_SHARED
     # a member whose row lists other pages for the shared keys
     x = _groups_case(99, 128, 2, 16, [20, 30], [64, 64], [(0, 2, 64)])
