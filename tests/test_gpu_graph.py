@@ -176,3 +176,39 @@ def test_padded_replay_at_a_fixed_maximum_batch(fused):
     got_k = k.view(torch.int16).cpu().numpy().view(np.uint16).reshape(-1, Hkv, d)
     got_v = v.view(torch.int16).cpu().numpy().view(np.uint16).reshape(-1, Hkv, d)
     assert np.array_equal(got_k, want_k) and np.array_equal(got_v, want_v)
+
+
+def test_shared_prefix_prefill_graph_replay():
+    """The shared-prefix prefill captured once and replayed twice: the same
+    output as the eager call, bit for bit, and the work-queue counters left
+    zeroed (the eager call after the replays is still correct)."""
+    from synth import share_prefix
+    x = make_inputs(seed=64, Hq=16, Hkv=8, d=128, page_size=16, new_lens=[40, 90, 7, 130, 60],
+                    prefix_lens=[256, 300, 256, 400, 10])
+    x = share_prefix(x, [(0, 4, 256)])
+    from tests.gpu_util import Run
+    r = Run(x).store()
+    eager = r.prefill_shared()
+    torch.cuda.synchronize()
+    assert int(r.status.item()) == 0
+    gs, gl = to_dev(x.meta["prefix_group_start"]), to_dev(x.meta["prefix_len"])
+    cu64 = x.cu_seqlens_q.astype(np.int64)
+    starts = x.meta["prefix_group_start"]
+    max_group = int(max(cu64[starts[g + 1]] - cu64[starts[g]] for g in range(len(starts) - 1)))
+    out = torch.empty_like(eager)
+    ws = pkv.prefill_workspace()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        pkv.paged_prefill_attn_shared(r.q, r.cu, r.k, r.v, r.page_table, r.seq_lens, x.scale,
+                                      x.max_q_len, gs, gl, max_group, workspace=ws,
+                                      dev_status=r.status, out=out, stream=s)
+    for _ in range(2):
+        out.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert int(r.status.item()) == 0
+        assert torch.equal(out.view(torch.int16), eager.view(torch.int16))
+    assert int(ws.view(torch.int32)[:3].abs().sum().item()) == 0
+    assert max_err(as_f64(out), oracle.run_inputs(x)) <= TOL
