@@ -16,15 +16,17 @@
 // decreasing work, heaviest first (its first item by block index, the rest
 // from a queue counter in the caller's workspace), so the last items to
 // finish are light ones, and the next item's Q and first K/V tiles load while
-// the current item finishes.  Roles (320 threads):
+// the current item finishes.  Roles (384 threads):
 //   warp 8      producer: takes the next item and publishes it to the other
-//               roles through a 2-slot ring; per item the Q tiles A and B,
-//               then 128-key K and V tiles through 2-stage rings, K one tile
-//               ahead of V.  Pages of >= 8 tokens come in as TMA boxes (one
-//               per page and 64-column block, 128-byte swizzle, straight into
-//               the layout the tensor core reads); smaller pages are gathered
-//               by the warp's lanes with 16-byte loads and swizzled stores.
-//               Page ids are read in warp-wide windows, one window ahead.
+//               roles through a 2-slot ring, and loads the Q tiles A and B.
+//   warps 8, 10, 11  loaders: 128-key K and V tiles through a 2-stage K ring
+//               and a 3-stage V ring, K one tile ahead of V, each warp
+//               copying its share of a tile's pages.  Pages of >= 8 tokens
+//               come in as TMA boxes (one per page and 64-column block,
+//               128-byte swizzle, straight into the layout the tensor core
+//               reads); smaller pages are gathered by the lanes with 16-byte
+//               loads and swizzled stores.  Page ids are read in warp-wide
+//               windows, one window ahead.
 //   warp 9      allocates all 512 TMEM columns (per query tile: a 128x128
 //               fp32 score buffer S, whose first 64 columns then hold P as
 //               bf16 pairs, and a 128 x head_dim fp32 output accumulator O)
@@ -50,6 +52,15 @@
 //               are all past the request's last token does no arithmetic.
 // While one tile's softmax runs, the tensor core works on the other tile's PV
 // and QK^T, so the two tiles take turns on the tensor core.
+//
+// Shared-prefix mode (pkv_paged_prefill_attn_shared): requests that share the
+// first S cached keys form a group, and an item is a block of the group's
+// new tokens packed densely over its requests.  The item first runs the S
+// shared keys (read through the first member's page row) for all its rows,
+// unmasked, then each member's private keys S .. L_r - 1, causal for that
+// member's rows and masked out for the rest; the online softmax carries
+// every row across both phases.  A shared K/V tile is thus read once per
+// item instead of once per request.
 #include <math.h>
 
 #include <atomic>
