@@ -302,7 +302,11 @@ __global__ void __launch_bounds__(kThreads, G <= 4 ? kCtasPerSm : 1)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     grid_dependency_wait();  // the pool rows of this step are written by the kernel before
-    allow_dependents();      // the merge kernel may become resident and wait for us
+    // No early trigger for the merge kernel: its blocks would become resident
+    // at once and sit on every SM until this grid ends, which keeps a
+    // whole-SM kernel on another stream (the prefill of a mixed step) from
+    // starting, and the standalone call measured no faster with them.  The
+    // merge kernel is released as this grid's blocks exit.
     if (tid == 0) {
         // full: the producer's arrival with the tx bytes
         for (int s = 0; s < STAGES; ++s) {
