@@ -443,14 +443,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         // (all but the newest group when keep_one), makes them visible to the
         // tensor core and arrives on that barrier.
         uint32_t gather_pending = 0;
-        // small pages: the key rows a loader lane copies, KPI keys per warp
-        // instruction, instructions li, li + 3, ... of a tile
+        // small pages: a warp instruction copies KPI whole key rows, one
+        // 16-byte piece per lane (lane = sub-row x CHK + piece); each 32-key
+        // block of a tile takes IPB instructions, and loader li issues
+        // instructions li, li + 3, ... of every block.  So the block, the key
+        // offsets and the swizzle terms are compile-time but for a per-lane
+        // base, and a copy costs a shuffle for its pool row, the address
+        // arithmetic and the copy itself.
         constexpr int CHK = D / 8;                // 16-byte pieces of a row
         constexpr int KPI = 32 / CHK;             // keys per warp instruction
-        constexpr int NGRP = BN / KPI;            // instructions per tile
-        constexpr int NIT = (NGRP + kLoaders - 1) / kLoaders;
+        constexpr int IPB = 32 / KPI;             // instructions per 32-key block
+        constexpr int UPB = (IPB + kLoaders - 1) / kLoaders;  // of them per loader, at most
         static_assert(BN == 128, "the page ids of a tile's keys are held 4 per lane");
-        int gpg[4], gpg_next[4];  // page ids of keys lane + 32 r of this tile / the next tile
+        const int ch = lane % CHK;                          // this lane's 16-byte piece
+        const int key_lane = li * KPI + lane / CHK;         // its key in the block, u = 0
+        const uint32_t dst_lane = static_cast<uint32_t>((ch >> 3) * BN * 128 + key_lane * 128);
+        const int64_t row_elems = static_cast<int64_t>(Hkv) * D;  // pool row stride (elements)
+        // pool rows (slots) of keys lane + 32 r of this tile, -1 where a key has
+        // none (past the row's keys, or a page id outside the pool); gpg_next
+        // holds the next tile's page ids as read, converted when it is issued
+        int gpg[4], gpg_next[4];
         auto flush_gather = [&](bool keep_one) {
             if (!gather_pending) return;
             if (keep_one)
@@ -598,13 +610,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                 steps_begin(ck, itm, cu_seqlens, seq_lens);
                 cv = ck;
             }
-            // page ids of tile kt's keys lane + 32 r of `row` (Lr keys)
+            // page ids of tile kt's keys lane + 32 r of `row` (Lr keys), as read
             auto load_ids = [&](const int32_t *row, int Lr, int kt, int *dstp) {
 #pragma unroll
                 for (int r = 0; r < 4; ++r) {
                     const int kk = kt * BN + r * 32 + lane;
-                    dstp[r] = kk < Lr ? row[kk >> ps_log2] : 0;
+                    dstp[r] = kk < Lr ? row[kk >> ps_log2] : -1;
                 }
+            };
+            // page ids of tile kt -> pool rows (slot = page x page_size +
+            // offset; the host checks that every slot fits an int), -1 past
+            // the row's Lr keys; true if a key's page id lies outside the pool
+            auto to_slots = [&](int Lr, int kt, int *p) -> bool {
+                bool bad = false;
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    const int kk = kt * BN + r * 32 + lane;
+                    const int id = p[r];
+                    const bool ok_page = kk < Lr && id >= 0 && id < num_pages;
+                    bad |= kk < Lr && !ok_page;
+                    p[r] = ok_page ? (id << ps_log2) + (kk & ps_mask) : -1;
+                }
+                return bad;
             };
             // page ids in warp-wide windows of 32 page boxes, the next window
             // loaded ahead; a new row (kFused moves to another request's row)
@@ -695,13 +722,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // a tile complete while the warp issues its next tile; then
                     // the warp waits for them, orders them before the tensor
                     // core's reads and arrives (see flush_gather).
-                    const __nv_bfloat16 *base = kv ? v_cache : k_cache;
+                    const __nv_bfloat16 *src_lane = (kv ? v_cache : k_cache) + static_cast<int64_t>(g) * D + ch * 8;
                     // page ids of this tile's keys: loaded for K(j) (or
-                    // prefetched while V(j-1) was issued) and reused for V(j),
-                    // which prefetches those of tile j + 1
+                    // prefetched while V(j-1) was issued) and converted to
+                    // pool rows, then reused for V(j), which prefetches those
+                    // of tile j + 1
+                    bool bad = false;
                     if constexpr (MODE == kFused) {
                         // (the tile's row may change between tiles: no lookahead)
-                        if (kv == 0) load_ids(trow, tL, tkt, gpg);
+                        if (kv == 0) {
+                            load_ids(trow, tL, tkt, gpg);
+                            bad = to_slots(tL, tkt, gpg);
+                        }
                     } else if (kv == 0) {
                         if (j == 0) {
                             load_ids(prow, L, 0, gpg);
@@ -709,26 +741,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                             for (int r = 0; r < 4; ++r) gpg[r] = gpg_next[r];
                         }
+                        bad = to_slots(L, j, gpg);
                     } else if (j + 1 < itm.n_kt) {
                         load_ids(prow, L, j + 1, gpg_next);
                     }
-                    bool bad = false;
 #pragma unroll
-                    for (int it = 0; it < NIT; ++it) {
-                        const int m = li + kLoaders * it;
-                        if (m >= NGRP) break;
-                        const int key = m * KPI + lane / CHK, ch = lane % CHK;
-                        const int kk = key0 + key;
-                        // the instruction's keys lie in one 32-key block (warp-uniform)
-                        const int blk32 = (m * KPI) >> 5;
-                        const int held = blk32 == 0 ? gpg[0] : blk32 == 1 ? gpg[1] : blk32 == 2 ? gpg[2] : gpg[3];
-                        const int pg = __shfl_sync(0xffffffffu, held, key & 31);
-                        const bool in_seq = key < nkeys;
-                        const bool ok_page = in_seq && pg >= 0 && pg < num_pages;
-                        bad |= in_seq && !ok_page;
-                        const int64_t sl = ok_page ? ((int64_t)pg << ps_log2) + (kk & ps_mask) : 0;
-                        cp_async16(dst + swz_offset(key, ch, BN), base + (sl * Hkv + g) * D + ch * 8,
-                                   ok_page ? 16u : 0u);
+                    for (int b32 = 0; b32 < 4; ++b32) {
+#pragma unroll
+                        for (int u = 0; u < UPB; ++u) {
+                            if (li + kLoaders * u >= IPB) break;  // (warp-uniform)
+                            const int kl = key_lane + kLoaders * KPI * u;  // key in the block, < 32
+                            const int sl = __shfl_sync(0xffffffffu, gpg[b32], kl);
+                            const uint32_t off = static_cast<uint32_t>(
+                                b32 * 32 * 128 + kLoaders * KPI * u * 128 + (((ch ^ kl) & 7) << 4));
+                            cp_async16(dst + dst_lane + off, src_lane + max(sl, 0) * row_elems,
+                                       sl >= 0 ? 16u : 0u);
+                        }
                     }
                     cp_async_commit();
                     if (__any_sync(0xffffffffu, bad) && lane == 0) bad_flag[slot] = 1;
