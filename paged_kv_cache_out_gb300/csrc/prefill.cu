@@ -443,21 +443,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         // (all but the newest group when keep_one), makes them visible to the
         // tensor core and arrives on that barrier.
         uint32_t gather_pending = 0;
-        // small pages: a warp instruction copies KPI whole key rows, one
-        // 16-byte piece per lane (lane = sub-row x CHK + piece); each 32-key
-        // block of a tile takes IPB instructions, and loader li issues
-        // instructions li, li + 3, ... of every block.  So the block, the key
-        // offsets and the swizzle terms are compile-time but for a per-lane
-        // base, and a copy costs a shuffle for its pool row, the address
-        // arithmetic and the copy itself.
-        constexpr int CHK = D / 8;                // 16-byte pieces of a row
-        constexpr int KPI = 32 / CHK;             // keys per warp instruction
-        constexpr int IPB = 32 / KPI;             // instructions per 32-key block
+        // small pages: a step of the copy loop moves KPI = 4 whole key rows,
+        // 8 lanes per row, each lane its 16-byte piece of every 64-column
+        // block of the row; each 32-key block of a tile takes IPB steps, and
+        // loader li takes steps li, li + 3, ... of every block.  So the block,
+        // the key offsets and the swizzle terms are compile-time but for a
+        // per-lane base, and a step costs a shuffle for its pool row, the
+        // address arithmetic and one copy per 64-column block.
+        constexpr int KPI = 4;                    // keys per step
+        constexpr int IPB = 32 / KPI;             // steps per 32-key block
         constexpr int UPB = (IPB + kLoaders - 1) / kLoaders;  // of them per loader, at most
         static_assert(BN == 128, "the page ids of a tile's keys are held 4 per lane");
-        const int ch = lane % CHK;                          // this lane's 16-byte piece
-        const int key_lane = li * KPI + lane / CHK;         // its key in the block, u = 0
-        const uint32_t dst_lane = static_cast<uint32_t>((ch >> 3) * BN * 128 + key_lane * 128);
+        const int ch = lane % 8;                            // this lane's piece of a 128-byte block row
+        const int key_lane = li * KPI + lane / 8;           // its key in the block, u = 0
+        const uint32_t dst_lane = static_cast<uint32_t>(key_lane * 128);
         const int64_t row_elems = static_cast<int64_t>(Hkv) * D;  // pool row stride (elements)
         // pool rows (slots) of keys lane + 32 r of this tile, -1 where a key has
         // none (past the row's keys, or a page id outside the pool); gpg_next
@@ -752,10 +751,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                             if (li + kLoaders * u >= IPB) break;  // (warp-uniform)
                             const int kl = key_lane + kLoaders * KPI * u;  // key in the block, < 32
                             const int sl = __shfl_sync(0xffffffffu, gpg[b32], kl);
-                            const uint32_t off = static_cast<uint32_t>(
-                                b32 * 32 * 128 + kLoaders * KPI * u * 128 + (((ch ^ kl) & 7) << 4));
-                            cp_async16(dst + dst_lane + off, src_lane + max(sl, 0) * row_elems,
-                                       sl >= 0 ? 16u : 0u);
+                            const uint32_t d = dst + dst_lane +
+                                               static_cast<uint32_t>(b32 * 32 * 128 + kLoaders * KPI * u * 128 +
+                                                                     (((ch ^ kl) & 7) << 4));
+                            const __nv_bfloat16 *src = src_lane + max(sl, 0) * row_elems;
+                            const uint32_t nb = sl >= 0 ? 16u : 0u;
+#pragma unroll
+                            for (int blk = 0; blk < NBLK; ++blk)
+                                cp_async16(d + blk * Lo::KBLK, src + blk * 64, nb);
                         }
                     }
                     cp_async_commit();
