@@ -18,6 +18,8 @@
 //    rows for this KV head into shared memory with TMA tensor copies (one box
 //    of min(page_size, T) rows per page), through a ring of mbarrier-tracked
 //    stages.  K/V are streamed once, so the copies carry an L2 evict-first hint.
+//    Pages under 8 tokens are gathered four rows per copy (tile::gather4) by
+//    four producer warps, whose issue rate limits such copies.
 //  * Four consumer warps split every tile by rows: head_dim/8 lanes hold one
 //    16-byte slice of a row; each lane keeps the G query heads' slice of q in
 //    registers (pre-multiplied by scale*log2 e), reduces dot products with
@@ -34,7 +36,18 @@ namespace pkv {
 namespace decode {
 
 constexpr int kConsumerWarps = 4;
-constexpr int kThreads = (kConsumerWarps + 1) * 32;  // warps 0-3 consume, warp 4 produces
+// warps 0-3 (warpgroup 0) consume; warp 4 produces, and with pages under 8
+// tokens warps 5-7 produce too (below)
+constexpr int kProducerWarps = 4;
+constexpr int kThreads = (kConsumerWarps + kProducerWarps) * 32;
+// With two blocks per SM a block launches with 128 registers per thread; the
+// producers then give up all but kProducerRegs and the consumers take
+// kConsumerRegs (128 x (176 + 80) = 256 x 128, so the increase always finds
+// its registers).  With one block per SM (G = 8) nothing moves.
+constexpr int kConsumerRegs = 176, kProducerRegs = 80;
+static_assert(kConsumerWarps * 32 * kConsumerRegs + kProducerWarps * 32 * kProducerRegs <=
+                  kThreads * (65536 / (2 * kThreads)),
+              "register split exceeds the registers of a block at two blocks per SM");
 constexpr int kMaxBatch = 4096;
 constexpr int kCtasPerSm = 2;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -310,7 +323,8 @@ __global__ void __launch_bounds__(kThreads, G <= 4 ? kCtasPerSm : 1)
     if (tid == 0) {
         // full: the producer's arrival with the tx bytes
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(smem_u32(&bars[s]), 1u);
+            // full: each producer's arrival with its tx bytes
+            mbar_init(smem_u32(&bars[s]), box_rows < 8 ? static_cast<uint32_t>(kProducerWarps) : 1u);
             mbar_init(smem_u32(&bars[STAGES + s]), kConsumerWarps);  // empty: one per consumer warp
         }
         mbar_init(smem_u32(&bars[2 * STAGES]), kConsumerWarps);  // fused stores written
@@ -328,8 +342,20 @@ __global__ void __launch_bounds__(kThreads, G <= 4 ? kCtasPerSm : 1)
     const int64_t my_end = part.start(blockIdx.x + 1);
     if (my_start >= my_end) return;
 
-    if (warp == kConsumerWarps) {
-        // ------------------------------------------------------------ producer
+    if (warp >= kConsumerWarps) {
+        // ------------------------------------------------------------ producers
+        // Page boxes (pages of >= 8 tokens) take a few TMA copies per tile, all
+        // issued by warp 4.  Pages of fewer tokens take a tile::gather4 per
+        // four key rows, and a warp's TMA issue rate then limits the copy
+        // rate, so warps 4 and 5 issue half of the K gathers each (warp 4 also
+        // the q copy) and warps 6 and 7 those of V.  Measured on the page
+        // size 1 decode workloads, one issuing warp -> two -> four: Qwen3
+        // 290 -> 232 -> 233 us, long context (d 64) 135 -> 100 -> 89 us.
+        // (Warps splitting the page boxes too made long-context decode at
+        // page size 256 slower, 71.4 -> 73.0 us.)
+        const int pw = warp - kConsumerWarps;
+        if constexpr (G <= 4) regs_decrease<kProducerRegs>();
+        if (pw > 0 && box_rows >= 8) return;
         const uint64_t policy = l2_evict_first_policy();
         if (lane == 0) {
             prefetch_tmap(&kmap);
@@ -436,17 +462,18 @@ __global__ void __launch_bounds__(kThreads, G <= 4 ? kCtasPerSm : 1)
                 } else {
                     // pages of fewer than 8 tokens: the tile's key rows gathered
                     // four at a time with TMA (tile::gather4 over the pool viewed
-                    // as rows of one head, row = slot * Hkv + g).  Lane i < NG
-                    // copies K rows 4i..4i+3, then the same V rows (K and V in
-                    // separate instructions measured 1-2 % faster than one
-                    // instruction over both tensor maps).  Keys
+                    // as rows of one head, row = slot * Hkv + g).  Gather i < NG
+                    // (rows 4i..4i+3) of K is issued by lane i % NH of warp
+                    // 4 + i / NH, the same gather of V by the same lane of warp
+                    // 6 + i / NH.  Keys
                     // past the sequence end take the row of the tile's first key
                     // (the consumers never use them), so every row read exists.
                     constexpr int NG = T / 4;  // gathers per tile and tensor
-                    static_assert(NG <= 32, "one K and one V gather per lane");
+                    static_assert(NG % 2 == 0 && NG / 2 <= 32, "one gather per lane");
                     const int b0 = tile * bpt;
                     if (bpt <= 32 && (b0 >> 5) != w_cur) advance(b0 >> 5);
-                    const int gi = lane % NG;
+                    constexpr int NH = NG / 2;  // gathers per producer warp
+                    const int gi = (pw & 1) * NH + lane % NH;
                     int rows[4];
                     bool bad = false;
 #pragma unroll
@@ -464,18 +491,18 @@ __global__ void __launch_bounds__(kThreads, G <= 4 ? kCtasPerSm : 1)
                     }
                     bad = __any_sync(0xffffffffu, bad);
                     if (lane == 0) {
-                        flags[s] = bad ? 1 : 0;
-                        mbar_arrive_expect_tx(full, (bad ? 0u : 2u * S::TILE_BYTES) + q_bytes);
+                        if (pw == 0) flags[s] = bad ? 1 : 0;
+                        mbar_arrive_expect_tx(full, (bad ? 0u : static_cast<uint32_t>(S::TILE_BYTES / 2)) +
+                                                        (pw == 0 ? q_bytes : 0u));
                     }
                     __syncwarp();
-                    if (!bad && lane < NG) {
-                        const uint32_t dst = smem_u32(st) + gi * 4 * D * 2;
-                        tma_gather4(dst, &kmap, full, 0, rows[0], rows[1], rows[2], rows[3], policy);
-                        tma_gather4(dst + S::TILE_BYTES, &vmap, full, 0, rows[0], rows[1], rows[2], rows[3],
+                    if (!bad && lane < NH) {
+                        const uint32_t dst = smem_u32(st) + (pw < 2 ? 0u : S::TILE_BYTES) + gi * 4 * D * 2;
+                        tma_gather4(dst, pw < 2 ? &kmap : &vmap, full, 0, rows[0], rows[1], rows[2], rows[3],
                                     policy);
                     }
                 }
-                if (first && lane == 0)
+                if (first && lane == 0 && pw == 0)
                     bulk_load(smem_u32(st + 2 * S::TILE_BYTES),
                               q + ((int64_t)p.b * Hq + (int64_t)p.g * G) * D, G * D * 2, full);
             }
@@ -484,6 +511,7 @@ __global__ void __launch_bounds__(kThreads, G <= 4 ? kCtasPerSm : 1)
     }
 
     // ---------------------------------------------------------------- consumers
+    if constexpr (G <= 4) regs_increase<kConsumerRegs>();
     const int grp = warp * S::ROWS_PER_WARP + lane / R;  // row-group of this lane
     const int lr = lane % R;                             // slice of a row
     // the lane owns 16-byte chunks lr, lr + R, ... of each row
