@@ -31,6 +31,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import math
 import os
@@ -92,9 +93,15 @@ def measured_peaks():
 
 
 def source_digest(*names) -> str:
+    """Digest of the named kernel sources with comments and whitespace removed,
+    so that a profile's recorded figures stay valid across comment edits and
+    are dropped by any change to the code."""
     h = hashlib.sha256()
     for n in names:
-        h.update(open(os.path.join(ROOT, "paged_kv_cache_out_gb300", "csrc", n), "rb").read())
+        text = open(os.path.join(ROOT, "paged_kv_cache_out_gb300", "csrc", n)).read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 
