@@ -59,6 +59,16 @@ def test_many_short_sequences():
     check(decode_case(32, lens, Hq=16, Hkv=8, d=128, ps=16))
 
 
+@pytest.mark.parametrize("d,Hq", [(128, 16), (64, 32)])
+@pytest.mark.parametrize("ps", [1, 16])
+def test_maximum_batch(d, Hq, ps):
+    # 4096 sequences: the per-sequence arrays in shared memory leave room for
+    # one block per SM, which still splits its registers between consumers
+    # and producers; page size 1 has all four producer warps gathering
+    lens = np.random.default_rng(33).integers(1, 49, size=4096)
+    check(decode_case(33, lens, Hq=Hq, Hkv=8, d=d, ps=ps), threads=16)
+
+
 def test_single_token_sequence_returns_its_value():
     x = decode_case(33, [1], Hq=8, Hkv=2, d=64, ps=16)
     out, _ = check(x)
