@@ -41,26 +41,33 @@ constexpr int kConsumerWarps = 4;
 constexpr int kProducerWarps = 4;
 constexpr int kThreads = (kConsumerWarps + kProducerWarps) * 32;
 // With two blocks per SM a block launches with 128 registers per thread; the
-// producers then give up all but kProducerRegs and the consumers take
-// kConsumerRegs (128 x (176 + 80) = 256 x 128, so the increase always finds
-// its registers).  With one block per SM (G = 8) nothing moves.
-constexpr int kConsumerRegs = 176, kProducerRegs = 80;
-static_assert(kConsumerWarps * 32 * kConsumerRegs + kProducerWarps * 32 * kProducerRegs <=
-                  kThreads * (65536 / (2 * kThreads)),
-              "register split exceeds the registers of a block at two blocks per SM");
+// producers then give up all but RegSplit::producer and the consumers take
+// RegSplit::consumer (128 x (176 + 80) = 256 x 128, so the increase always
+// finds its registers).  With one block per SM (G = 8) nothing moves.  Head
+// size 64 with 4 query heads per KV head keeps 16 elements per lane (below)
+// and takes 184 (measured: long-context decode 71.0 -> 69.4 us at page size
+// 256, 89.3 -> 83.9 us at page size 1).
+template <int D, int G>
+struct RegSplit {
+    static constexpr int consumer = (D == 64 && G == 4) ? 184 : 176;
+    static constexpr int producer = 256 - consumer;
+    static_assert(kConsumerWarps * 32 * consumer + kProducerWarps * 32 * producer <=
+                      kThreads * (65536 / (2 * kThreads)),
+                  "register split exceeds the registers of a block at two blocks per SM");
+};
 constexpr int kMaxBatch = 4096;
 constexpr int kCtasPerSm = 2;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kNegBig = -1.0e30f;  // running-max start: finite, so 2^(m - m') never is NaN
 
 // A consumer lane owns EPL elements of a row (EPL/8 16-byte chunks): 16 when
-// there are at most 2 query heads per KV head (fewer lanes per row, so fewer
-// shuffle levels to reduce the dot products), else 8, which keeps 4 heads
-// within the registers of two blocks per SM.
+// there are at most 2 query heads per KV head, or 4 at head size 64 (fewer
+// lanes per row, so fewer shuffle levels to reduce the dot products), else 8,
+// which keeps the heads within the registers of two blocks per SM.
 template <int D, int G>
 struct Shape {
     static constexpr int T = (D == 128) ? 32 : 64;  // key tokens per tile
-    static constexpr int EPL = (G <= 2) ? 16 : 8;    // elements per lane
+    static constexpr int EPL = (G <= 2 || (G == 4 && D == 64)) ? 16 : 8;  // elements per lane
     static constexpr int NCH = EPL / 8;               // 16-byte chunks per lane
     static constexpr int R = D / EPL;                 // lanes per K/V row
     static constexpr int ROWS_PER_WARP = 32 / R;
@@ -354,7 +361,7 @@ __global__ void __launch_bounds__(kThreads, G <= 4 ? kCtasPerSm : 1)
         // (Warps splitting the page boxes too made long-context decode at
         // page size 256 slower, 71.4 -> 73.0 us.)
         const int pw = warp - kConsumerWarps;
-        if constexpr (G <= 4) regs_decrease<kProducerRegs>();
+        if constexpr (G <= 4) regs_decrease<RegSplit<D, G>::producer>();
         if (pw > 0 && box_rows >= 8) return;
         const uint64_t policy = l2_evict_first_policy();
         if (lane == 0) {
@@ -511,7 +518,7 @@ __global__ void __launch_bounds__(kThreads, G <= 4 ? kCtasPerSm : 1)
     }
 
     // ---------------------------------------------------------------- consumers
-    if constexpr (G <= 4) regs_increase<kConsumerRegs>();
+    if constexpr (G <= 4) regs_increase<RegSplit<D, G>::consumer>();
     const int grp = warp * S::ROWS_PER_WARP + lane / R;  // row-group of this lane
     const int lr = lane % R;                             // slice of a row
     // the lane owns 16-byte chunks lr, lr + R, ... of each row
