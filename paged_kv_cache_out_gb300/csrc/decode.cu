@@ -43,13 +43,15 @@ constexpr int kThreads = (kConsumerWarps + kProducerWarps) * 32;
 // With two blocks per SM a block launches with 128 registers per thread; the
 // producers then give up all but RegSplit::producer and the consumers take
 // RegSplit::consumer (128 x (176 + 80) = 256 x 128, so the increase always
-// finds its registers).  With one block per SM (G = 8) nothing moves.  Head
-// size 64 with 4 query heads per KV head keeps 16 elements per lane (below)
-// and takes 184 (measured: long-context decode 71.0 -> 69.4 us at page size
-// 256, 89.3 -> 83.9 us at page size 1).
+// finds its registers).  With one block per SM (G = 8) nothing moves.  With
+// 4 query heads per KV head the consumers keep 16 elements per lane (below)
+// and take 184 (measured: long-context decode, head size 64, 71.0 -> 69.4 us
+// at page size 256 and 89.3 -> 83.9 us at page size 1; head size 128,
+// 64 sequences of 512-4096 keys, 119.1 -> 113.8 us at page size 16 and
+// 142.6 -> 134.2 us at page size 1).
 template <int D, int G>
 struct RegSplit {
-    static constexpr int consumer = (D == 64 && G == 4) ? 184 : 176;
+    static constexpr int consumer = (G == 4) ? 184 : 176;
     static constexpr int producer = 256 - consumer;
     static_assert(kConsumerWarps * 32 * consumer + kProducerWarps * 32 * producer <=
                       kThreads * (65536 / (2 * kThreads)),
@@ -61,13 +63,13 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kNegBig = -1.0e30f;  // running-max start: finite, so 2^(m - m') never is NaN
 
 // A consumer lane owns EPL elements of a row (EPL/8 16-byte chunks): 16 when
-// there are at most 2 query heads per KV head, or 4 at head size 64 (fewer
-// lanes per row, so fewer shuffle levels to reduce the dot products), else 8,
-// which keeps the heads within the registers of two blocks per SM.
+// there are at most 4 query heads per KV head (fewer lanes per row, so fewer
+// shuffle levels to reduce the dot products), else 8, which keeps 8 heads
+// within the registers of one block per SM.
 template <int D, int G>
 struct Shape {
     static constexpr int T = (D == 128) ? 32 : 64;  // key tokens per tile
-    static constexpr int EPL = (G <= 2 || (G == 4 && D == 64)) ? 16 : 8;  // elements per lane
+    static constexpr int EPL = (G <= 4) ? 16 : 8;  // elements per lane
     static constexpr int NCH = EPL / 8;               // 16-byte chunks per lane
     static constexpr int R = D / EPL;                 // lanes per K/V row
     static constexpr int ROWS_PER_WARP = 32 / R;
