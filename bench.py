@@ -92,13 +92,14 @@ def measured_peaks():
     return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
 
 
-def source_digest(*names) -> str:
+def source_digest(*names, src_dir=None) -> str:
     """Digest of the named kernel sources with comments and whitespace removed,
     so that a profile's recorded figures stay valid across comment edits and
     are dropped by any change to the code."""
+    src_dir = src_dir or os.path.join(ROOT, "paged_kv_cache_out_gb300", "csrc")
     h = hashlib.sha256()
     for n in names:
-        text = open(os.path.join(ROOT, "paged_kv_cache_out_gb300", "csrc", n)).read()
+        text = open(os.path.join(src_dir, n)).read()
         text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
         text = re.sub(r"//[^\n]*", " ", text)
         h.update(" ".join(text.split()).encode())
