@@ -20,8 +20,9 @@
 //    stages.  K/V are streamed once, so the copies carry an L2 evict-first hint.
 //    Pages under 8 tokens are gathered four rows per copy (tile::gather4) by
 //    four producer warps, whose issue rate limits such copies.
-//  * Four consumer warps split every tile by rows: head_dim/8 lanes hold one
-//    16-byte slice of a row; each lane keeps the G query heads' slice of q in
+//  * Four consumer warps split every tile by rows: head_dim/16 lanes hold one
+//    32-byte slice of a row each (head_dim/8 lanes, 16 bytes, with 8 query
+//    heads per KV head); each lane keeps the G query heads' slice of q in
 //    registers (pre-multiplied by scale*log2 e), reduces dot products with
 //    warp shuffles, keeps its own online-softmax state per head, and
 //    accumulates its slice of the output.  At the end of a segment piece the
