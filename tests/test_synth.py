@@ -91,3 +91,31 @@ def test_config_ranges(name, monkeypatch):
         assert new[:4].sum() == 1024 and (new[:4] >= 1).all() and (pre[:4] <= 2048).all()
         assert (new[4:] == 1).all() and len(new) == 260
         assert L[4:].min() >= 1 and L[4:].max() <= 8192
+
+
+def test_share_prefix_aliases_pages_and_partitions_the_batch():
+    from synth import make_inputs
+    from synth.workloads import share_prefix
+    B, ps = 8, 16
+    x = make_inputs(seed=3, Hq=4, Hkv=2, d=64, page_size=ps, new_lens=np.full(B, 5, np.int64),
+                    prefix_lens=np.array([40, 48, 33, 64, 50, 32, 47, 36], np.int64))
+    before = x.page_table.copy()
+    x = share_prefix(x, [(1, 4, 32), (5, 7, 16)])
+    starts = x.meta["prefix_group_start"].tolist()
+    lens = x.meta["prefix_len"].tolist()
+    # groups: {0}, {1,2,3} sharing 32 tokens, {4}, {5,6} sharing 16, {7}
+    assert starts == [0, 1, 4, 5, 7, 8] and lens == [0, 32, 0, 16, 0]
+    for first, end, shared in ((1, 4, 32), (5, 7, 16)):
+        for r in range(first, end):
+            assert (x.page_table[r, :shared // ps] == before[first, :shared // ps]).all()
+            assert (x.page_table[r, shared // ps:] == before[r, shared // ps:]).all()
+    for r in (0, 4, 7):
+        assert (x.page_table[r] == before[r]).all()
+    # every new token's slot lies in a page its own row still holds past the shared part
+    for b in range(B):
+        L = int(x.prefix_lens[b] + x.new_lens[b])
+        pages = set(x.page_table[b, :(L + ps - 1) // ps].tolist())
+        shared_pages = set(x.page_table[b, :lens[next(i for i in range(len(lens)) if starts[i] <= b < starts[i + 1])] // ps].tolist())
+        t0 = int(x.cu_seqlens_q[b])
+        for slot in x.out_loc[t0:t0 + int(x.new_lens[b])].tolist():
+            assert slot // ps in pages and slot // ps not in shared_pages
